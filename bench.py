@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one kda_chunk_fwd over the prefill workload B=8, T=8192, H=32,
+dk=dv=128 (bf16 q/k/v/o, fp32 g/beta/states, h0 ~ N(0, 0.02^2), hT returned).
+The same run also times the batched decode workload (256 sequences x H=32,
+128x128 fp32 state updated in place, 1000 consecutive steps) and reports it
+in the "decode" object. Inputs are synthetic (seeded), already resident in
+HBM for `value`; `e2e` repeats the prefill step through the same C-ABI call
+with pinned host buffers and the host<->device copies inside the timed region.
+
+Prints ONE JSON line (rank 0). Under torchrun (N > 1) every rank runs its own
+independent batch on its own GPU (data-parallel sequences, no collective on
+the data path): `value` = tokens of all ranks / max over ranks of the time.
+
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_57_gb300 import inputs  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (B=8,T=8192,H=32,d=128,bf16) & decode GB/s; % of roofline"
+PREFILL = inputs.PREFILL_B8_T8K
+DECODE = inputs.DECODE_N256
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+KERNEL_SOURCES = {
+    "prefill": "gated_delta_rule_57_gb300/csrc/kda_chunk_tc.cu",
+    "decode": "gated_delta_rule_57_gb300/csrc/kda_decode.cu",
+}
+
+
+# --------------------------------------------------------------------------
+# algorithmic traffic (bytes the method must move, nothing more)
+# --------------------------------------------------------------------------
+def prefill_bytes(w, B=None):
+    B = w.B if B is None else B
+    th = B * w.T * w.H
+    esz = 2 if w.io == "bf16" else 4
+    per_th = esz * (2 * w.dk + 2 * w.dv) + 4 * w.dk + 4  # q, k, v, o + g + beta
+    states = 2 * B * w.H * w.dk * w.dv * 4 if w.h0_std is not None else B * w.H * w.dk * w.dv * 4
+    return th * per_th + states
+
+
+def decode_bytes(w):
+    nh = w.N * w.H
+    esz = 2 if w.io == "bf16" else 4
+    return nh * (2 * w.dk * w.dv * 4 + esz * (2 * w.dk + 2 * w.dv) + 4 * w.dk + 4)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def file_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(which):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the capture; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(which)
+    if not d or d.get("source_sha256_16") != file_sha(KERNEL_SOURCES[which]):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], None, set()
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (weak scaling: one independent batch per rank)
+# --------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base, rank):
+    return base + 7919 * rank
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def time_prefill(x, steps, warmup, world, device):
+    from gated_delta_rule_57_gb300 import kda
+    w = PREFILL
+    o = torch.empty_like(x["v"])
+    hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o=o, hT=hT,
+                          stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, launch_ms, o, hT
+
+
+def time_prefill_e2e(xh, steps, warmup, device):
+    """Same step through the public call, from pinned host memory and back."""
+    from gated_delta_rule_57_gb300 import kda
+    w = PREFILL
+    names = ("q", "k", "v", "g", "beta", "h0")
+    xd = {n: torch.empty_like(xh[n], device=device) for n in names}
+    o_d = torch.empty_like(xd["v"])
+    hT_d = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=device)
+    o_h = torch.empty_like(o_d, device="cpu").pin_memory()
+    hT_h = torch.empty_like(hT_d, device="cpu").pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(xh[n].numel() * xh[n].element_size() for n in names)
+    d2h = o_h.numel() * o_h.element_size() + hT_h.numel() * hT_h.element_size()
+
+    def step():
+        for n in names:
+            xd[n].copy_(xh[n], non_blocking=True)
+        kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"], o=o_d,
+                          hT=hT_d, stream=stream)
+        o_h.copy_(o_d, non_blocking=True)
+        hT_h.copy_(hT_d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def time_decode(device, seed, warmup=10):
+    from gated_delta_rule_57_gb300 import kda
+    w = DECODE
+    x = inputs.decode_inputs(w, device, seed=seed)
+    S = x["S"]
+    o = torch.empty(w.N, w.H, w.dv, dtype=inputs.io_dtype(w.io), device=device)
+    stream = torch.cuda.current_stream()
+    for s in range(warmup):
+        kda.kda_decode_step(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], S, o=o,
+                            stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(w.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(w.steps):
+        ev[s][0].record(stream)
+        kda.kda_decode_step(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], S, o=o,
+                            stream=stream)
+        ev[s][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    per = [a.elapsed_time(b) for a, b in ev]
+    return total / w.steps, statistics.mean(per), w.steps
+
+
+def oracle_sample(budget_s, max_b=None):
+    """Oracle on whole batch rows of the prefill workload until ~budget_s."""
+    import oracle
+    w = PREFILL
+    rows = w.B if max_b is None else max_b
+    tokens, elapsed, done = 0, 0.0, 0
+    for b in range(rows):
+        x = inputs.prefill_inputs(w, "cpu", B=1, seed=w.seed + 101 * b)
+        t0 = time.perf_counter()
+        oracle.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+        elapsed += time.perf_counter() - t0
+        tokens += w.T
+        done += 1
+        if elapsed >= budget_s:
+            break
+    return tokens, elapsed, done
+
+
+def run_ours(args):
+    rank, world, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from gated_delta_rule_57_gb300 import kda
+    kda.lib()  # fail loudly now if the CUDA library is missing
+    w = PREFILL
+    x = inputs.prefill_inputs(w, device, seed=rank_seed(w.seed, rank))
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        total_ms, launch_ms, _, _ = time_prefill(x, args.steps, args.warmup, world, device)
+    clocks = clk.summary()
+    ms_step = max_over_ranks(total_ms / args.steps, world, device)
+    tokens_per_rank = w.B * w.T
+    value = world * tokens_per_rank / (ms_step * 1e-3)
+
+    peaks, peak_src = load_peaks()
+    alg_bytes = prefill_bytes(w)
+    launch_avg = statistics.mean(launch_ms)
+    achieved = alg_bytes / (launch_avg * 1e-3) / 1e9
+    traffic = recorded_traffic("prefill")
+
+    # end to end through the same call, pinned host buffers, copies timed
+    xh = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "h0")}
+    e2e_ms, h2d, d2h = time_prefill_e2e(xh, max(3, min(args.steps, 20)), 2, device)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    del xh
+
+    dec_ms, dec_launch_ms, dec_steps = time_decode(device, rank_seed(DECODE.seed, rank))
+    dec_bytes = decode_bytes(DECODE)
+    dec_gbs = world * dec_bytes / (max_over_ranks(dec_ms, world, device) * 1e-3) / 1e9
+    dec_ach = dec_bytes / (dec_launch_ms * 1e-3) / 1e9
+    dec_traffic = recorded_traffic("decode")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        tok, el, rows = oracle_sample(args.cpu_budget)
+        cpu = {"value": tok / el, "unit": "tokens/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{rows} of {w.B} batch rows x T={w.T} x H={w.H} (fp64 token loop, "
+                         f"{el:.1f} s wall)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk,
+                       "dv": w.dv, "io": "bf16 q/k/v/o, fp32 g/beta/h0/hT",
+                       "global_batch": world * w.B, "seq_len": w.T,
+                       "parallelism": f"dp{world} (independent sequences per GPU)",
+                       "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.2f} GB per step)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic, "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "kernel": "kda_chunk_fwd (prefill)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * tokens_per_rank / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "decode": {"workload": DECODE.name, "value": dec_gbs, "unit": "GB/s",
+                       "ms_per_step": dec_ms, "steps": dec_steps,
+                       "roofline": {"bound": "hbm", "achieved": dec_ach,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": dec_ach / peaks["hbm_gbs"],
+                                    "traffic": dec_traffic,
+                                    "algorithmic_bytes_per_launch": dec_bytes},
+                       "gpu_launches": dec_steps,
+                       "l2": f"state larger than L2 ({dec_bytes / 1e9:.2f} GB per step)"},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# --------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    w = PREFILL
+    per_step_rows = 1  # one batch row (8192 tokens x 32 heads) per step
+    for i in range(args.warmup):
+        oracle_sample(0.0, max_b=per_step_rows)
+    times = []
+    for i in range(args.steps):
+        tok, el, _ = oracle_sample(0.0, max_b=per_step_rows)
+        times.append(el)
+    ms = 1e3 * statistics.mean(times)
+    val = w.T * per_step_rows / (ms * 1e-3)
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: 1 of {w.B} batch rows x T={w.T} x H={w.H}"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

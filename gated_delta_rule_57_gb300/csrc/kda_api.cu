@@ -1,0 +1,164 @@
+// C ABI of the KDA library: argument validation and dispatch to the kernels.
+//
+// Everything here runs on the host, allocates nothing and never synchronises.
+// Argument errors return before any CUDA call is made.
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+void set_last_error(const char* msg) {
+    strncpy(g_last_error, msg, sizeof(g_last_error) - 1);
+    g_last_error[sizeof(g_last_error) - 1] = '\0';
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// [p, p + n) and [q, q + m) overlap (both non-empty)?
+bool overlaps(const void* p, size_t n, const void* q, size_t m) {
+    if (!p || !q || n == 0 || m == 0) return false;
+    uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + m && b < a + n;
+}
+
+// n = a * b * c * d with overflow detection (all factors >= 0).
+bool mul_ok(size_t* out, size_t a, size_t b, size_t c = 1, size_t d = 1) {
+    const size_t lim = (size_t)1 << 62;
+    size_t r = a;
+    for (size_t f : {b, c, d}) {
+        if (f != 0 && r > lim / f) return false;
+        r *= f;
+    }
+    *out = r;
+    return true;
+}
+
+kda_status_t fail(kda_status_t s, const char* why) {
+    set_last_error(why);
+    return s;
+}
+
+kda_status_t check_dims(int dk, int dv, kda_dtype_t io) {
+    if (dk <= 0 || dv <= 0) return fail(KDA_ERR_INVALID_ARG, "dk and dv must be positive");
+    if (io != KDA_BF16 && io != KDA_F32) return fail(KDA_ERR_INVALID_ARG, "unknown io dtype");
+    if (dk != dv) return fail(KDA_ERR_UNSUPPORTED, "dk != dv is not implemented");
+    if (dk != 64 && dk != 128) return fail(KDA_ERR_UNSUPPORTED, "dk must be 64 or 128");
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char* kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_DECAY_RANGE: return "KDA_ERR_DECAY_RANGE";
+        case KDA_ERR_NONFINITE: return "KDA_ERR_NONFINITE";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error_string(void) { return g_last_error; }
+
+size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dtype_t io) {
+    if (B < 0 || T < 0 || H < 0) return (size_t)-1;
+    if (check_dims(dk, dv, io) != KDA_OK) return (size_t)-1;
+    return 0;  // both prefill paths keep their intermediates on chip
+}
+
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* h0, void* o, float* hT, int B,
+                           int T, int H, int dk, int dv, kda_dtype_t io, void* workspace,
+                           size_t ws_bytes, int* d_status, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
+    kda_status_t st = check_dims(dk, dv, io);
+    if (st != KDA_OK) return st;
+    if ((long long)B * H >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "B*H too large");
+    if (B == 0 || H == 0) return KDA_OK;
+    const size_t esz = io == KDA_BF16 ? 2 : 4;
+    size_t n_qk, n_v, n_b, n_s;
+    if (!mul_ok(&n_qk, B, T, H, dk) || !mul_ok(&n_v, B, T, H, dv) || !mul_ok(&n_b, B, T, H) ||
+        !mul_ok(&n_s, B, H, dk, dv))
+        return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta and o must be non-NULL");
+    const void* ptrs[] = {q, k, v, g, h0, o, hT};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (beta && !aligned4(beta)) return fail(KDA_ERR_INVALID_ARG, "beta must be 4-byte aligned");
+    // o and hT are written while the inputs are still being read.
+    const void* ins[] = {q, k, v, g, beta, h0};
+    const size_t in_bytes[] = {n_qk * esz, n_qk * esz, n_v * esz, n_qk * 4, n_b * 4,
+                               h0 ? n_s * 4 : 0};
+    for (int i = 0; i < 6; i++) {
+        if (overlaps(o, n_v * esz, ins[i], in_bytes[i]))
+            return fail(KDA_ERR_INVALID_ARG, "o overlaps an input");
+        if (i < 5 && overlaps(hT, n_s * 4, ins[i], in_bytes[i]))
+            return fail(KDA_ERR_INVALID_ARG, "hT overlaps an input other than h0");
+    }
+    if (h0 && hT && h0 != hT && overlaps(hT, n_s * 4, h0, n_s * 4))
+        return fail(KDA_ERR_INVALID_ARG, "hT partially overlaps h0");
+    if (overlaps(o, n_v * esz, hT, n_s * 4)) return fail(KDA_ERR_INVALID_ARG, "o overlaps hT");
+
+    kda::ChunkFwdArgs a{q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, d_status,
+                        static_cast<cudaStream_t>(stream)};
+    cudaError_t e = io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
+                                   : kda::launch_chunk_fwd_simt(a, io);
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float* S, void* o, int N, int H, int dk,
+                             int dv, kda_dtype_t io, int* d_status, void* stream) {
+    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
+    kda_status_t st = check_dims(dk, dv, io);
+    if (st != KDA_OK) return st;
+    if ((long long)N * H >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "N*H too large");
+    if (N == 0 || H == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !S || !o)
+        return fail(KDA_ERR_INVALID_ARG, "all decode pointers must be non-NULL");
+    const void* ptrs[] = {q, k, v, g, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (!aligned4(beta)) return fail(KDA_ERR_INVALID_ARG, "beta must be 4-byte aligned");
+    const size_t esz = io == KDA_BF16 ? 2 : 4;
+    size_t n_k, n_v, n_s;
+    if (!mul_ok(&n_k, N, H, dk) || !mul_ok(&n_v, N, H, dv) || !mul_ok(&n_s, N, H, dk, dv))
+        return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+    const void* ins[] = {q, k, v, g, beta};
+    const size_t in_bytes[] = {n_k * esz, n_k * esz, n_v * esz, n_k * 4, (size_t)N * H * 4};
+    for (int i = 0; i < 5; i++) {
+        if (overlaps(o, n_v * esz, ins[i], in_bytes[i]) || overlaps(S, n_s * 4, ins[i], in_bytes[i]))
+            return fail(KDA_ERR_INVALID_ARG, "o or S overlaps an input");
+    }
+    if (overlaps(o, n_v * esz, S, n_s * 4)) return fail(KDA_ERR_INVALID_ARG, "o overlaps S");
+    kda::DecodeArgs a{q, k, v, g, beta, S, o, N, H, dk, dv, d_status,
+                      static_cast<cudaStream_t>(stream)};
+    cudaError_t e = kda::launch_decode(a, io);
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Internal declarations shared by the KDA CUDA translation units.
+// Not part of the public ABI (include/kda.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Launch parameters common to both chunked-forward paths. Pointers are device
+// pointers; layouts as documented in kda.h.
+struct ChunkFwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    const float* h0;  // may be null
+    void* o;
+    float* hT;  // may be null
+    int B, T, H, dk, dv;
+    int* d_status;  // may be null
+    cudaStream_t stream;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    float* S;
+    void* o;
+    int N, H, dk, dv;
+    int* d_status;
+    cudaStream_t stream;
+};
+
+// Each launcher returns cudaSuccess or the launch error.
+cudaError_t launch_chunk_fwd_simt(const ChunkFwdArgs& a, kda_dtype_t io);
+cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a);
+cudaError_t launch_decode(const DecodeArgs& a, kda_dtype_t io);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// Lower log-decay bound (section "A lower bound that deleted a GPU code path"
+// of the orkas.ai page "Kimi K3 architecture": at least 0.67% ~ e^-5 of the
+// state survives one step).
+constexpr float kLogDecayMin = -5.0f;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Status bits for one log-decay value: range [-5, 0] and finiteness.
+__device__ __forceinline__ int decay_flags(float gv) {
+    int f = 0;
+    if (!(fabsf(gv) <= 3.402823466e38f)) f |= KDA_DEV_NONFINITE;  // NaN or Inf
+    else if (gv < kLogDecayMin || gv > 0.0f) f |= KDA_DEV_DECAY_RANGE;
+    return f;
+}
+__device__ __forceinline__ int finite_flag(float x) {
+    return (fabsf(x) <= 3.402823466e38f) ? 0 : KDA_DEV_NONFINITE;
+}
+
+// OR a per-thread flag word into *d_status with one atomic per warp.
+__device__ __forceinline__ void report_flags(int* d_status, int flags) {
+    unsigned m = __activemask();
+    int any = __reduce_or_sync(m, flags);
+    if (any && d_status && (threadIdx.x & 31) == (__ffs(m) - 1)) atomicOr(d_status, any);
+}
+
+}  // namespace kda

@@ -1,0 +1,161 @@
+"""Thin Python binding of the KDA C ABI (``include/kda.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libkda.so``. PyTorch provides device memory and streams. There is
+no CPU fallback: if the library is missing or a tensor is not on a CUDA
+device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_DECAY_RANGE = 5
+KDA_ERR_NONFINITE = 6
+KDA_ERR_TIMEOUT = 7
+
+KDA_BF16 = 0
+KDA_F32 = 1
+
+KDA_DEV_DECAY_RANGE = 0x1
+KDA_DEV_NONFINITE = 0x2
+KDA_DEV_TIMEOUT = 0x4
+
+_DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(what)
+
+
+def header_functions():
+    """Names of the functions declared in include/kda.h."""
+    with open(os.path.join(_build.INCLUDE, "kda.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"\b(kda_\w+)\s*\(", text)
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libkda.so (building it first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if build_if_missing and _build.is_stale():
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"KDA CUDA library not built: {path} is missing")
+            L = ctypes.CDLL(path)
+            vp, I, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.kda_abi_version.argtypes = []
+            L.kda_abi_version.restype = I
+            L.kda_status_string.argtypes = [I]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_last_error_string.argtypes = []
+            L.kda_last_error_string.restype = ctypes.c_char_p
+            L.kda_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I]
+            L.kda_chunk_fwd_workspace_size.restype = sz
+            L.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, vp,
+                                        sz, vp, vp]
+            L.kda_chunk_fwd.restype = I
+            L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
+            L.kda_decode_step.restype = I
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().kda_status_string(code).decode()
+
+
+def _check(code: int):
+    if code != KDA_OK:
+        L = lib()
+        raise KdaError(code, f"{status_string(code)}: {L.kda_last_error_string().decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("KDA tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("KDA tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def kda_chunk_fwd_workspace_size(B: int, T: int, H: int, dk: int, dv: int,
+                                 io: torch.dtype = torch.bfloat16) -> int:
+    n = lib().kda_chunk_fwd_workspace_size(B, T, H, dk, dv, _DTYPE[io])
+    if n == ctypes.c_size_t(-1).value:
+        raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size")
+    return int(n)
+
+
+def kda_chunk_fwd(q, k, v, g, beta, h0=None, *, o=None, hT=None, want_hT: bool = True,
+                  status: Optional[torch.Tensor] = None, workspace=None, stream=None):
+    """KDA chunked forward. q, k, g: [B,T,H,dk]; v: [B,T,H,dv]; beta: [B,T,H].
+
+    Returns (o, hT); hT is None when want_hT is False and no hT is given.
+    `status` (a CUDA int32 tensor with one element) receives the OR of the
+    KDA_DEV_* flags.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = kda_chunk_fwd_workspace_size(B, T, H, dk, dv, q.dtype)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                               _ptr(o), _ptr(hT), B, T, H, dk, dv, io, _ptr(workspace),
+                               ws_bytes, _ptr(status), _stream(stream))
+    _check(code)
+    return o, hT
+
+
+def kda_decode_step(q, k, v, g, beta, S, *, o=None, status: Optional[torch.Tensor] = None,
+                    stream=None):
+    """One in-place decode step. q, k, g: [N,H,dk]; v: [N,H,dv]; beta: [N,H];
+    S: [N,H,dk,dv] fp32 (updated in place). Returns o [N,H,dv]."""
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    code = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S),
+                                 _ptr(o), N, H, dk, dv, io, _ptr(status), _stream(stream))
+    _check(code)
+    return o

@@ -1,0 +1,144 @@
+/*
+ * kda.h — C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) library.
+ *
+ * KDA is the linear-attention layer of the Kimi K3 architecture described on
+ * the orkas.ai page "Kimi K3 architecture" (and its translations; the poyo.ai
+ * page "Kimi K3 architecture" summarises it under "What is Kimi Delta
+ * Attention?"). Per head it keeps a fixed-size state S (dk x dv, fp32) with a
+ * per-channel decay and a token-dependent transition:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * (section "Sequence: three quarters of the layers stopped reading
+ * everything": a fixed-size state that decays; section "The bill arrives in
+ * the serving stack": serial update, token-dependent transition of the
+ * incoming state, in-place update while decoding). The log-decay is bounded,
+ * g in [-5, 0] (section "A lower bound that deleted a GPU code path": at
+ * least 0.67% of the state survives each step, so a 16-token tile's
+ * cumulative log-decay stays above -80).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer owned by the caller. The library
+ *     never allocates, frees or synchronises; work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*; NULL means the legacy default stream).
+ *   - Tensors are contiguous and row-major; every pointer is 16-byte aligned
+ *     except beta, which needs 4 bytes:
+ *       q, k, g : [B, T, H, dk]      v, o : [B, T, H, dv]      beta : [B, T, H]
+ *       h0, hT  : [B, H, dk, dv]     (decode: T = 1 and B = N, S = [N, H, dk, dv])
+ *   - q, k, v, o have type `io` (bf16 or fp32); g, beta and states are fp32.
+ *   - No scaling is applied to q: o = S^T q exactly. Callers that want
+ *     1/sqrt(dk) pre-scale q.
+ *   - Supported sizes: dk = dv in {64, 128}; any T >= 0 (ragged tails are
+ *     handled; T = 0 writes hT = h0); B, H, N >= 0 (zero launches nothing)
+ *     with B*H, N*H < 2^31 and every tensor under 2^62 elements.
+ *
+ * Errors
+ *   - Argument errors are reported synchronously by the return value and
+ *     nothing is launched.
+ *   - A failed launch returns KDA_ERR_CUDA; kda_last_error_string() then
+ *     names the CUDA error (the library links its own CUDA runtime, so the
+ *     caller's cudaGetLastError does not see it).
+ *   - Data-dependent conditions are OR-ed, as the KDA_DEV_* bits below, into
+ *     the device int `*d_status` when d_status is not NULL. The computation
+ *     still runs to completion. The caller reads the word after its own
+ *     synchronisation and clears it before reuse.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misaligned pointer */
+    KDA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. dk != dv) */
+    KDA_ERR_WORKSPACE = 3,   /* workspace pointer or size too small */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    KDA_ERR_DECAY_RANGE = 5, /* (device) some g outside [-5, 0] */
+    KDA_ERR_NONFINITE = 6,   /* (device) NaN or Inf in g or beta */
+    KDA_ERR_TIMEOUT = 7      /* (device) a bounded on-chip wait gave up */
+} kda_status_t;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
+
+/* Bits OR-ed into *d_status by the kernels. */
+#define KDA_DEV_DECAY_RANGE 0x1 /* some g < -5 or g > 0 */
+#define KDA_DEV_NONFINITE 0x2   /* some g or beta is NaN or Inf */
+#define KDA_DEV_TIMEOUT 0x4     /* an mbarrier wait exceeded its iteration cap */
+
+/* Version of this header the library was built from (KDA_ABI_VERSION). */
+int kda_abi_version(void);
+
+/* Static string naming a status code; never NULL. */
+const char* kda_status_string(kda_status_t s);
+
+/* Why the last call on this host thread failed ("" if none did); never NULL. */
+const char* kda_last_error_string(void);
+
+/*
+ * Bytes of device workspace kda_chunk_fwd needs for this problem. The current
+ * kernels keep everything on chip and return 0; callers should still query it
+ * and pass a buffer at least this large (NULL is accepted when it is 0).
+ * Returns (size_t)-1 for arguments kda_chunk_fwd would reject.
+ */
+size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dtype_t io);
+
+/*
+ * Chunked forward (prefill) of KDA over B sequences of T tokens and H heads.
+ *
+ * Computes, for every (b, h), the recurrence above over t = 0..T-1 starting
+ * from S_{-1} = h0[b, h] (zeros when h0 is NULL), writes o[b, t, h, :] = o_t
+ * and, when hT is not NULL, hT[b, h] = S_{T-1}. Internally the sequence is
+ * processed in chunks with 16-token decay tiles (the "divide by the
+ * accumulated decay" blockwise evaluation of section "A lower bound that
+ * deleted a GPU code path"); the result equals the token-by-token recurrence
+ * up to rounding.
+ *
+ *   q, k   : [B, T, H, dk] of type io          (in)
+ *   v      : [B, T, H, dv] of type io          (in)
+ *   g      : [B, T, H, dk] fp32 log-decay      (in; must lie in [-5, 0])
+ *   beta   : [B, T, H]     fp32                (in)
+ *   h0     : [B, H, dk, dv] fp32 or NULL       (in)
+ *   o      : [B, T, H, dv] of type io          (out; must not alias inputs)
+ *   hT     : [B, H, dk, dv] fp32 or NULL       (out; may alias h0)
+ *   workspace, ws_bytes : see kda_chunk_fwd_workspace_size
+ *   d_status : device int or NULL              (in/out, OR-ed KDA_DEV_* bits)
+ *   stream : cudaStream_t
+ *
+ * io = KDA_BF16 runs the tensor-core (tcgen05/TMEM) path with fp32 state;
+ * io = KDA_F32 runs an fp32 CUDA-core path for high-accuracy callers.
+ */
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* h0, void* o, float* hT, int B,
+                           int T, int H, int dk, int dv, kda_dtype_t io, void* workspace,
+                           size_t ws_bytes, int* d_status, void* stream);
+
+/*
+ * One decode step for N sequences (one token each), state updated in place
+ * (section "The bill arrives in the serving stack", third bullet: the state
+ * is overwritten where it lives).
+ *
+ *   q, k : [N, H, dk] of type io;  v : [N, H, dv] of type io
+ *   g    : [N, H, dk] fp32;        beta : [N, H] fp32
+ *   S    : [N, H, dk, dv] fp32, read as S_{t-1} and overwritten with S_t
+ *   o    : [N, H, dv] of type io,  o = S_t^T q
+ *   d_status, stream : as for kda_chunk_fwd
+ *
+ * HBM-bandwidth bound: each call reads and writes S once.
+ */
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float* S, void* o, int N, int H, int dk,
+                             int dv, kda_dtype_t io, int* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

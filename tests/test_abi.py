@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/kda.h
+declares, and rejects bad arguments before making any CUDA call.
+
+No call here reaches a kernel: every argument set is invalid, so validation
+returns first. These run without a GPU.
+"""
+import ctypes
+import re
+
+import pytest
+
+from gated_delta_rule_57_gb300 import build, kda
+
+ST = kda
+
+
+@pytest.fixture(scope="module")
+def L():
+    return kda.lib()
+
+
+def test_exports_every_header_symbol(L):
+    names = kda.header_functions()
+    assert {"kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+            "kda_status_string", "kda_abi_version", "kda_last_error_string"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"libkda.so does not export {n}"
+
+
+def test_abi_version_matches_header(L):
+    text = open(build.INCLUDE + "/kda.h").read()
+    ver = int(re.search(r"#define KDA_ABI_VERSION (\d+)", text).group(1))
+    assert L.kda_abi_version() == ver
+
+
+def test_status_enum_matches_header():
+    text = open(build.INCLUDE + "/kda.h").read()
+    for name, val in re.findall(r"(KDA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text):
+        assert getattr(kda, name) == int(val), name
+        assert kda.status_string(int(val)) == name
+    for name, val in re.findall(r"#define (KDA_DEV_\w+) (0x[0-9a-f]+)", text):
+        assert getattr(kda, name) == int(val, 16), name
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+
+
+def test_workspace_size(L):
+    assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 128, 128, kda.KDA_BF16) == 0
+    bad = ctypes.c_size_t(-1).value
+    assert L.kda_chunk_fwd_workspace_size(1, 16, 1, 96, 96, kda.KDA_BF16) == bad
+    assert L.kda_chunk_fwd_workspace_size(1, 16, 1, 128, 64, kda.KDA_F32) == bad
+    assert L.kda_chunk_fwd_workspace_size(-1, 16, 1, 128, 128, kda.KDA_F32) == bad
+    assert L.kda_chunk_fwd_workspace_size(1, 16, 1, 64, 64, 7) == bad
+
+
+# Fake, 16-byte aligned addresses: never dereferenced, validation rejects first.
+A = [0x10000 * (i + 1) for i in range(8)]
+
+
+def call_fwd(L, q=A[0], k=A[1], v=A[2], g=A[3], beta=A[4], h0=None, o=A[5], hT=A[6], B=1,
+             T=16, H=1, dk=64, dv=64, io=kda.KDA_BF16):
+    return L.kda_chunk_fwd(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, None, 0, None,
+                           None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), ST.KDA_ERR_INVALID_ARG),
+    (dict(T=-3), ST.KDA_ERR_INVALID_ARG),
+    (dict(dk=96, dv=96), ST.KDA_ERR_UNSUPPORTED),
+    (dict(dk=128, dv=64), ST.KDA_ERR_UNSUPPORTED),
+    (dict(dk=0, dv=0), ST.KDA_ERR_INVALID_ARG),
+    (dict(io=5), ST.KDA_ERR_INVALID_ARG),
+    (dict(q=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(beta=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(o=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(k=A[1] + 8), ST.KDA_ERR_INVALID_ARG),     # misaligned
+    (dict(beta=A[4] + 2), ST.KDA_ERR_INVALID_ARG),  # beta needs 4 bytes
+    (dict(o=A[0]), ST.KDA_ERR_INVALID_ARG),         # o aliases q
+    (dict(hT=A[3]), ST.KDA_ERR_INVALID_ARG),        # hT aliases g
+    (dict(B=1 << 16, H=1 << 16), ST.KDA_ERR_INVALID_ARG),  # B*H >= 2^31
+])
+def test_chunk_fwd_rejects(L, kw, code):
+    assert call_fwd(L, **kw) == code
+    assert L.kda_last_error_string()  # a reason is recorded
+
+
+def test_empty_batch_is_a_no_op(L):
+    # B = 0 or H = 0: nothing to do, nothing launched, even with NULL pointers.
+    assert L.kda_chunk_fwd(None, None, None, None, None, None, None, None, 0, 16, 4, 64, 64,
+                           kda.KDA_BF16, None, 0, None, None) == ST.KDA_OK
+    assert L.kda_decode_step(None, None, None, None, None, None, None, 0, 4, 128, 128,
+                             kda.KDA_F32, None, None) == ST.KDA_OK
+
+
+def call_dec(L, q=A[0], k=A[1], v=A[2], g=A[3], beta=A[4], S=A[5], o=A[6], N=2, H=1, dk=128,
+             dv=128, io=kda.KDA_BF16):
+    return L.kda_decode_step(q, k, v, g, beta, S, o, N, H, dk, dv, io, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=-1), ST.KDA_ERR_INVALID_ARG),
+    (dict(dk=32, dv=32), ST.KDA_ERR_UNSUPPORTED),
+    (dict(S=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(o=A[2]), ST.KDA_ERR_INVALID_ARG),
+    (dict(S=A[5] + 4), ST.KDA_ERR_INVALID_ARG),
+    (dict(io=3), ST.KDA_ERR_INVALID_ARG),
+])
+def test_decode_rejects(L, kw, code):
+    assert call_dec(L, **kw) == code

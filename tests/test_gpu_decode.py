@@ -1,0 +1,71 @@
+"""GPU parity of kda_decode_step against the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_57_gb300 import inputs, kda
+from helpers import assert_o, assert_s
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_steps(w, steps, **kw):
+    x = inputs.decode_inputs(w, DEV, steps=steps, **kw)
+    S = x["S"].clone()
+    S_ref = x["S"].double().cpu().numpy()
+    dt = inputs.io_dtype(w.io)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for s in range(steps):
+        o = kda.kda_decode_step(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], S,
+                                status=status)
+        torch.cuda.synchronize()
+        o_ref, S_ref = oracle.decode(x["q"][s].cpu(), x["k"][s].cpu(), x["v"][s].cpu(),
+                                     x["g"][s].cpu(), x["beta"][s].cpu(), S_ref)
+        assert_o(o, o_ref, dt, f"o at step {s}")
+    assert_s(S, S_ref, dt, "S")
+    assert int(status.item()) == 0
+
+
+def test_workload_n256_first_steps():
+    run_steps(inputs.DECODE_N256, 3)
+
+
+@pytest.mark.parametrize("io,d", [("bf16", 64), ("f32", 128), ("f32", 64)])
+def test_small_decode(io, d):
+    w = inputs.DecodeWorkload("small", 5, 3, d, d, io, 11, 4)
+    run_steps(w, 4)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_decode_continues_prefill(io):
+    """Prefill T tokens, then decode token T: equals prefill of T + 1 tokens."""
+    w = inputs.PrefillWorkload("small", 3, 41, 2, 128, 128, io, 12, h0_std=0.02)
+    x = inputs.prefill_inputs(w, DEV)
+    T = 40
+    o_full, h_full = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    part = {n: x[n][:, :T].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    _, S = kda.kda_chunk_fwd(part["q"], part["k"], part["v"], part["g"], part["beta"], x["h0"])
+    last = {n: x[n][:, T].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    o_dec = kda.kda_decode_step(last["q"], last["k"], last["v"], last["g"], last["beta"], S)
+    torch.cuda.synchronize()
+    xc = {n: t.cpu() for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    dt = inputs.io_dtype(io)
+    assert_o(o_dec, o_ref[:, T], dt, "decoded token")
+    assert_s(S, h_ref, dt, "state after decode")
+    assert_o(o_full[:, T], o_ref[:, T], dt, "prefill token")
+
+
+@pytest.mark.parametrize("bad,flag", [(-7.0, kda.KDA_DEV_DECAY_RANGE),
+                                      (float("inf"), kda.KDA_DEV_NONFINITE)])
+def test_decode_status_flags(bad, flag):
+    w = inputs.DecodeWorkload("small", 4, 2, 128, 128, "bf16", 13, 1)
+    x = inputs.decode_inputs(w, DEV)
+    x["g"][0, 2, 1, 100] = bad
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_decode_step(x["q"][0], x["k"][0], x["v"][0], x["g"][0], x["beta"][0], x["S"],
+                        status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & flag

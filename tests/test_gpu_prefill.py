@@ -1,0 +1,190 @@
+"""GPU parity of kda_chunk_fwd against the fp64 oracle (through the C ABI)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_57_gb300 import inputs, kda
+from helpers import assert_o, assert_s
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def small(io, d, h0):
+    return inputs.PrefillWorkload("small", 1, 1, 1, d, d, io, 0, h0_std=0.02 if h0 else None)
+
+
+def run_case(w, *, B=None, T=None, H=None, seed=None, device_gen=False, h0_override=None):
+    gen_dev = DEV if device_gen else "cpu"
+    x = inputs.prefill_inputs(w, gen_dev, B=B, T=T, H=H, seed=seed)
+    if h0_override is not None:
+        x["h0"] = h0_override
+    xd = {n: (t.to(DEV) if t is not None else None) for n, t in x.items()}
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, hT = kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"],
+                              status=status)
+    torch.cuda.synchronize()
+    return x, o, hT, int(status.item())
+
+
+def check_against_oracle(x, o, hT, dtype):
+    o_ref, h_ref = oracle.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    eo = assert_o(o, o_ref, dtype)
+    eh = assert_s(hT, h_ref, dtype)
+    return eo, eh
+
+
+def test_tiny_f32_workload():
+    x, o, hT, st = run_case(inputs.TINY_F32)
+    assert st == 0
+    check_against_oracle(x, o, hT, torch.float32)
+
+
+CASES = [
+    # (B, T, H, d, io, h0): several chunks, ragged tails, tiny T, both head sizes
+    (2, 200, 3, 128, "bf16", True),
+    (1, 1, 2, 64, "bf16", False),
+    (1, 15, 1, 128, "f32", True),
+    (1, 17, 2, 64, "f32", False),
+    (1, 250, 2, 64, "bf16", True),
+    (3, 64, 2, 128, "bf16", False),
+    (1, 129, 1, 128, "f32", True),
+    (2, 333, 2, 128, "f32", False),
+    (1, 1000, 4, 128, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("B,T,H,d,io,h0", CASES)
+def test_small_cases(B, T, H, d, io, h0):
+    w = small(io, d, h0)
+    x, o, hT, st = run_case(w, B=B, T=T, H=H, seed=B * 1000 + T + H + d)
+    assert st == 0
+    check_against_oracle(x, o, hT, inputs.io_dtype(io))
+
+
+def test_workload_t4096_stress_heads():
+    """Heads 16..31 decay at g = -4.99 everywhere: a 16-token tile reaches
+    e^-79.84, the edge the bounded-reciprocal diagonal tiles must survive."""
+    x, o, hT, st = run_case(inputs.PREFILL_T4K, device_gen=True)
+    assert st == 0
+    check_against_oracle(x, o, hT, torch.bfloat16)
+
+
+@pytest.mark.slow
+def test_workload_b8_t8192():
+    x, o, hT, st = run_case(inputs.PREFILL_B8_T8K, device_gen=True)
+    assert st == 0
+    check_against_oracle(x, o, hT, torch.bfloat16)
+
+
+@pytest.mark.slow
+def test_workload_t1m_sampled_heads():
+    """T = 2^20: the full batch runs on the GPU; the oracle recomputes two
+    heads over the whole sequence and every output of those heads is checked."""
+    w = inputs.PREFILL_T1M
+    x = inputs.prefill_inputs(w, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, hT = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    heads = [3, 28]
+    sub = {n: x[n][:, :, heads].contiguous().cpu() for n in ("q", "k", "v", "g", "beta")}
+    o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None,
+                                  nthreads=len(heads))
+    assert_o(o[:, :, heads], o_ref, torch.bfloat16)
+    assert_s(hT[:, heads], h_ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_empty_sequence_returns_h0(io):
+    w = small(io, 128, True)
+    x = inputs.prefill_inputs(w, DEV, B=2, T=0, H=3)
+    o, hT = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    torch.cuda.synchronize()
+    assert o.numel() == 0
+    assert torch.equal(hT, x["h0"])
+    _, hz = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(hz) == 0
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_hT_may_alias_h0(io):
+    w = small(io, 64, True)
+    x = inputs.prefill_inputs(w, DEV, B=2, T=100, H=2, seed=5)
+    o1, h1 = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    h = x["h0"].clone()
+    o2, h2 = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h, hT=h)
+    torch.cuda.synchronize()
+    assert h2.data_ptr() == h.data_ptr()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_chaining_matches_single_pass(io):
+    """Prefill [0, T1) then [T1, T) with hT -> h0 equals one pass over [0, T)."""
+    w = small(io, 128, True)
+    x = inputs.prefill_inputs(w, DEV, B=2, T=300, H=2, seed=6)
+    o, hT = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    T1 = 137
+    p1 = {n: x[n][:, :T1].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    p2 = {n: x[n][:, T1:].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    o1, h1 = kda.kda_chunk_fwd(p1["q"], p1["k"], p1["v"], p1["g"], p1["beta"], x["h0"])
+    o2, h2 = kda.kda_chunk_fwd(p2["q"], p2["k"], p2["v"], p2["g"], p2["beta"], h1)
+    torch.cuda.synchronize()
+    dt = inputs.io_dtype(io)
+    xc = {n: (t.cpu() if t is not None else None) for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(torch.cat([o1, o2], 1), o_ref, dt, "chained o")
+    assert_s(h2, h_ref, dt, "chained hT")
+    assert_o(o, o_ref, dt)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("gval", [0.0, -5.0])
+def test_decay_edges(io, gval):
+    """g = 0 (no forgetting) and g = -5 (the bound itself) everywhere."""
+    w = small(io, 128, True)
+    x = inputs.prefill_inputs(w, "cpu", B=1, T=160, H=2, seed=7)
+    x["g"].fill_(gval)
+    xd = {n: t.to(DEV) for n, t in x.items()}
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, hT = kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"],
+                              status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check_against_oracle(x, o, hT, inputs.io_dtype(io))
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_beta_zero_pure_decay(io):
+    w = small(io, 64, True)
+    x = inputs.prefill_inputs(w, "cpu", B=1, T=70, H=2, seed=8)
+    x["beta"].zero_()
+    xd = {n: t.to(DEV) for n, t in x.items()}
+    o, hT = kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"])
+    torch.cuda.synchronize()
+    ref = torch.exp(x["g"].double().sum(1))[..., None] * x["h0"].double()
+    assert_s(hT, ref.numpy(), inputs.io_dtype(io))
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("bad,flag", [(-6.0, kda.KDA_DEV_DECAY_RANGE),
+                                      (0.5, kda.KDA_DEV_DECAY_RANGE),
+                                      (float("nan"), kda.KDA_DEV_NONFINITE)])
+def test_status_flags(io, bad, flag):
+    w = small(io, 64, False)
+    x = inputs.prefill_inputs(w, DEV, B=1, T=40, H=2, seed=9)
+    x["g"][0, 33, 1, 5] = bad
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & flag
+    status.zero_()
+    x["g"][0, 33, 1, 5] = -1.0
+    kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
