@@ -1,0 +1,42 @@
+"""Run the hot path on one named workload, for profilers.
+
+    python -m gated_delta_rule_57_gb300.profile_cases prefill [--B 8] [--calls 4]
+    python -m gated_delta_rule_57_gb300.profile_cases decode  [--calls 4]
+
+Draws the seeded synthetic inputs on the GPU, then makes `calls` back-to-back
+calls of kda_chunk_fwd (prefill: B x 8192 tokens x 32 heads, d = 128, bf16)
+or kda_decode_step (256 sequences x 32 heads, d = 128). Under a profiler,
+skip the first calls as warm-up (e.g. ncu -s 2 -c 1 -k regex:kda_).
+"""
+import argparse
+
+import torch
+
+from . import inputs, kda
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("which", choices=["prefill", "decode"])
+    ap.add_argument("--B", type=int, default=8)
+    ap.add_argument("--calls", type=int, default=4)
+    args = ap.parse_args()
+    dev = torch.device("cuda", 0)
+    if args.which == "prefill":
+        w = inputs.PREFILL_B8_T8K
+        x = inputs.prefill_inputs(w, dev, B=args.B)
+        o = torch.empty_like(x["v"])
+        hT = torch.empty(args.B, w.H, w.dk, w.dv, device=dev)
+        for _ in range(args.calls):
+            kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o=o, hT=hT)
+    else:
+        w = inputs.DECODE_N256
+        x = inputs.decode_inputs(w, dev, steps=args.calls)
+        for s in range(args.calls):
+            kda.kda_decode_step(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], x["S"])
+    torch.cuda.synchronize()
+    print(f"{args.which}: {args.calls} calls done")
+
+
+if __name__ == "__main__":
+    main()
