@@ -24,15 +24,15 @@
 //   round 4  D1    += [-W; Qt - PW] * S0   ->  D1 = [U; O]
 //   round 5  S     += Kb^T * U              (S pre-scaled by e^{G_C} in TMEM)
 //
-// Execution. One CTA per (b, h) sequence, 256 threads, ~204 KB of shared
-// memory (one CTA per SM), 416 TMEM columns: the fp32 state S (128 lanes x
-// 128 columns) stays in tensor memory for the whole sequence. Inputs arrive by
-// TMA (q, k, v with the 128-byte swizzle the MMA descriptors expect; g as a
-// plain fp32 tile); the next chunk's g, q/k and v are prefetched as soon as
-// their buffers are free. One thread issues the MMAs; completion is signalled
-// through mbarriers whose waits are bounded (timeout -> KDA_DEV_TIMEOUT).
-// Intermediates never leave the SM: the kernel reads each input once and
-// writes o (and hT) once.
+// Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
+// lane quarter), ~207 KB of shared memory (one CTA per SM), 416 TMEM columns:
+// the fp32 state S (128 lanes x 128 columns) stays in tensor memory for the
+// whole sequence. Inputs arrive by TMA with the 128-byte swizzle (q, k, v in
+// the layout the MMA descriptors expect; g in 32-channel blocks); the next
+// chunk's g, q/k, v and beta are prefetched as soon as their buffers are free.
+// One thread issues the MMAs; completion is signalled through mbarriers whose
+// waits are bounded (timeout -> KDA_DEV_TIMEOUT). Intermediates never leave
+// the SM: the kernel reads each input once and writes o (and hT) once.
 #include <cudaTypedefs.h>
 
 #include "kda_internal.cuh"
@@ -43,12 +43,13 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kC = 64;     // chunk length
-constexpr int kD = 128;    // dk = dv
-constexpr int kThreads = 256;
+constexpr int kC = 64;          // chunk length
+constexpr int kD = 128;         // dk = dv
+constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (bytes from a 1024-aligned base).
-constexpr uint32_t OFF_G = 0;          // g tile, fp32 [64][128], plain
+constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; then decay constants
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
 constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch | A1
 constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
@@ -59,17 +60,21 @@ constexpr uint32_t OFF_QT = 172032;    // Qt, SW128 64 x 128
 constexpr uint32_t OFF_U = 188416;     // U, SW128 64 x 128 (MN-major B)
 constexpr uint32_t OFF_BETA = 204800;  // fp32 [64]
 constexpr uint32_t OFF_LAM = 205056;   // fp32 [128]  e^{G_C}
-constexpr uint32_t OFF_GEND = 205568;  // fp32 [4][128] per-tile log-decay totals
+constexpr uint32_t OFF_GT = 205568;    // fp32 [4][128] tile log2-decay totals
 constexpr uint32_t SMEM_BYTES = 207616 + 1024;
-// aliases inside OFF_KM (live between round 1 and round 4)
-constexpr int LDF = 65;
-constexpr uint32_t OFF_FA = OFF_KM;           // fp32 A  [64][65]
-constexpr uint32_t OFF_FT = OFF_KM + 16640;   // fp32 T  [64][65]
-constexpr uint32_t OFF_MS = OFF_KM + 33280;   // fp32 3 x [16][17]
+// aliases inside OFF_KM (solve scratch lives between round 1 and round 2; A1
+// between round 3 and round 4)
+constexpr int LDA = 65;  // fp32 A: odd stride, column walks are conflict-free
+constexpr int LDT = 68;  // fp32 T: 16-byte rows for float4 strips
+constexpr int LDM = 52;
+constexpr uint32_t OFF_FA = OFF_KM;           // fp32 A [64][65]
+constexpr uint32_t OFF_FT = OFF_KM + 16640;   // fp32 T [64][68]
+constexpr uint32_t OFF_MS = OFF_KM + 34048;   // fp32 2 x [16][52] block-row partial products
 constexpr uint32_t OFF_A1 = OFF_KM;           // [-W; Q'], SW128 128 x 128
 constexpr uint32_t OFF_S = OFF_KT;            // S0 bf16, SW128 128 x 128 (MN-major B)
 constexpr int KM_ROWS = 160;                  // windows of 16, 32, 48, 64 rows
-__device__ __forceinline__ constexpr int win_row(int a) { return 8 * a * (a + 1); }  // 0,16,48,96
+__host__ __device__ __forceinline__ constexpr int win_row(int a) { return 8 * a * (a + 1); }
+static_assert(OFF_MS + 2 * 16 * LDM * 4 <= OFF_V, "solve scratch overflows the window buffer");
 
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
@@ -85,73 +90,111 @@ struct TcParams {
     int* d_status;
 };
 
+// 2^x on the SFU (ex2.approx, flush-to-zero). Arguments here are log2-decays
+// in [-116, 116]; results below 2^-126 are decays too small to matter.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
-    return __bfloat1622float2(v);
-}
-
-// Writes 8 consecutive bf16 (c0..c0+7, c0 % 8 == 0) of row r of an SW128 tile.
-__device__ __forceinline__ void st_row8(unsigned char* tile, int r, int c0, int R,
-                                        const float* x) {
+__device__ __forceinline__ uint4 pack8(const float* x) {
     uint4 u;
     u.x = pack_bf16(x[0], x[1]);
     u.y = pack_bf16(x[2], x[3]);
     u.z = pack_bf16(x[4], x[5]);
     u.w = pack_bf16(x[6], x[7]);
-    *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0, R)) = u;
+    return u;
+}
+// bf16 is the upper half of an fp32 word: widening is a shift or a mask.
+__device__ __forceinline__ void unpack8(uint4 u, float* x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// 8 consecutive bf16 (c0..c0+7, c0 % 8 == 0) of row r of an SW128 tile.
+__device__ __forceinline__ void st_row8(unsigned char* tile, int r, int c0, int R,
+                                        const float* x) {
+    *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0, R)) = pack8(x);
 }
 __device__ __forceinline__ void ld_row8(const unsigned char* tile, int r, int c0, int R,
                                         float* x) {
-    uint4 u = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0, R));
-    float2 f;
-    f = unpack_bf16(u.x); x[0] = f.x; x[1] = f.y;
-    f = unpack_bf16(u.y); x[2] = f.x; x[3] = f.y;
-    f = unpack_bf16(u.z); x[4] = f.x; x[5] = f.y;
-    f = unpack_bf16(u.w); x[6] = f.x; x[7] = f.y;
+    unpack8(*reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0, R)), x);
 }
 
-// Descriptors for the two operand orientations of an SW128 tile with R rows.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int R, int kk) {
-    return sdesc_sw128(base + (uint32_t)(kk >> 2) * (uint32_t)R * 128u + (uint32_t)(kk & 3) * 32u,
-                       16, 1024);
+// Descriptors for the two operand orientations of an SW128 tile with R rows;
+// k-step kk covers 16 elements of K. The start address is the low 14-bit
+// field (in 16-byte units), so advancing an operand is a plain add.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base) {
+    return sdesc_sw128(base, 16, 1024);
 }
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int R, int kk) {
-    return sdesc_sw128(base + (uint32_t)kk * 2048u, (uint32_t)R * 128u, 1024);
+__device__ __forceinline__ uint64_t kstep_kmajor(int R, int kk) {
+    return (uint64_t)(((uint32_t)(kk >> 2) * (uint32_t)R * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
 }
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int R) {
+    return sdesc_sw128(base, (uint32_t)R * 128u, 1024);
+}
+__device__ __forceinline__ uint64_t kstep_mnmajor(int kk) { return (uint64_t)(kk * 128); }
 
-// Gram readout for the rows of one 16-token tile: A (strict lower, scaled by
-// beta_r) into the fp32 solve buffer, P (lower incl. diagonal) into rows
-// 64..127 of A0. `v` holds this warp's TMEM window columns, `off` the offset of
-// this tile's window inside `v`.
-template <int TILE, int OFF>
-__device__ __forceinline__ void gram_rows(const float* v, int r, int part, float beta_r,
-                                          unsigned char* sm) {
-    constexpr int N = 16 * (TILE + 1);
-    if (part == 0) {
-        float* FA = reinterpret_cast<float*>(sm + OFF_FA) + r * LDF;
+// One block row of the blocked triangular inverse T = (I + A)^-1 (AB = 1..3):
+// with the diagonal blocks and block rows < AB known,
+//   M         = A[AB, <AB] T[<AB, <AB]    (16 x 16AB; K split in KS parts)
+//   T[AB,<AB] = -T[AB, AB] M
+// T is stored with zeros above the diagonal, so every loop has a compile-time
+// trip count and no predicate.
+template <int AB, int KS>
+__device__ __forceinline__ void merge_block_row(const float* FA, float* FT, float* MS, int tid) {
+    constexpr int RB = 16 * AB, NS = 4 * RB, KL = RB / KS;
+    if (tid < NS * KS) {
+        const int part = tid / NS, strip = tid % NS;
+        const int i = strip / (RB / 4), s0 = 4 * (strip % (RB / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* arow = FA + (RB + i) * LDA + part * KL;
+        const float* tcol = FT + part * KL * LDT + s0;
 #pragma unroll
-        for (int s = 0; s < kC; s++) {
-            float x = 0.f;
-            if (s < N) x = (s < r) ? beta_r * v[OFF + s] : 0.f;
-            FA[s] = x;
+        for (int m = 0; m < KL; m++) {
+            const float av = arow[m];
+            const float4 tv = *reinterpret_cast<const float4*>(tcol + m * LDT);
+            acc.x += av * tv.x;
+            acc.y += av * tv.y;
+            acc.z += av * tv.z;
+            acc.w += av * tv.w;
         }
-    } else {
-#pragma unroll
-        for (int c8 = 0; c8 < kC; c8 += 8) {
-            float x[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int s = c8 + j;
-                x[j] = 0.f;
-                if (s < N) x[j] = (s <= r) ? v[OFF + s] : 0.f;
-            }
-            st_row8(sm + OFF_A0, 64 + r, c8, 128, x);
-        }
+        *reinterpret_cast<float4*>(MS + part * 16 * LDM + i * LDM + s0) = acc;
     }
+    __syncthreads();
+    if (tid < NS) {
+        const int i = tid / (RB / 4), s0 = 4 * (tid % (RB / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* trow = FT + (RB + i) * LDT + RB;
+#pragma unroll
+        for (int m = 0; m < 16; m++) {
+            const float tv = trow[m];
+            float4 mv = *reinterpret_cast<const float4*>(MS + m * LDM + s0);
+            if (KS > 1) {
+                const float4 m2 = *reinterpret_cast<const float4*>(MS + 16 * LDM + m * LDM + s0);
+                mv.x += m2.x;
+                mv.y += m2.y;
+                mv.z += m2.z;
+                mv.w += m2.w;
+            }
+            acc.x += tv * mv.x;
+            acc.y += tv * mv.y;
+            acc.z += tv * mv.z;
+            acc.w += tv * mv.w;
+        }
+        *reinterpret_cast<float4*>(FT + (RB + i) * LDT + s0) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -166,13 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    // TMEM view of a warp: lane quarter q (lanes 32q..32q+31), column group u.
+    const int q = warp & 3, u = warp >> 2;
+    const int lane = 32 * q + (tid & 31);
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int T = p.T;
     const int nchunks = (T + kC - 1) / kC;
     const uint32_t sbase = smem_addr(sm);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* slam = reinterpret_cast<float*>(sm + OFF_LAM);
-    float* sgend = reinterpret_cast<float*>(sm + OFF_GEND);
+    float* sgt = reinterpret_cast<float*>(sm + OFF_GT);
     int flags = 0;
     bool failed = false;
 
@@ -194,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
+    const uint32_t tq = tmem_at(tbase, 32 * q, 0);  // this warp's lane quarter
 
     auto issue_qk = [&](int c) {
         mbar_arrive_expect_tx(&bars[BAR_QK], 4 * 8192);
@@ -205,7 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_g = [&](int c) {
         mbar_arrive_expect_tx(&bars[BAR_G], 32768);
-        tma_load_4d(sm + OFF_G, &map_g, &bars[BAR_G], 0, h, c * kC, b);
+#pragma unroll
+        for (int cbk = 0; cbk < 4; cbk++)
+            tma_load_4d(sm + OFF_G + cbk * 8192, &map_g, &bars[BAR_G], 32 * cbk, h, c * kC, b);
     };
     auto issue_v = [&](int c) {
         mbar_arrive_expect_tx(&bars[BAR_V], 2 * 8192);
@@ -217,14 +266,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_g(0);
         issue_v(0);
     }
+    // beta is strided by H in memory: plain loads, kept one chunk ahead.
+    auto load_beta = [&](int c) {
+        const int t = c * kC + tid;
+        return (tid < kC && c < nchunks && t < T) ? p.beta[((size_t)b * T + t) * p.H + h] : 0.f;
+    };
+    float beta_next = load_beta(0);
 
     // Incoming state -> TMEM (lane i = key channel i, column j = value channel j).
     {
-        const int lane = (warp & 3) * 32 + (tid & 31);
-        const int cbase = (warp >> 2) * 64;
-        const float* src = p.h0 ? p.h0 + ((size_t)blockIdx.x * kD + lane) * kD + cbase : nullptr;
+        const float* src = p.h0 ? p.h0 + ((size_t)blockIdx.x * kD + lane) * kD + 32 * u : nullptr;
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 16) {
+        for (int cc = 0; cc < 32; cc += 16) {
             float x[16];
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
@@ -232,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
             }
-            tmem_st16(tmem_at(tbase, (warp & 3) * 32, TM_S + cbase + cc), x);
+            tmem_st16(tq + TM_S + 32 * u + cc, x);
         }
         tmem_wait_st();
     }
@@ -253,93 +306,145 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = (uint32_t)(c & 1);
 
         // ------------------------------------------------------------ P1
+        // Warp = (tile a, 32-channel block cb); lane = (row pair j, 8-channel
+        // group). Log-decays are kept in log2 units: each exponential is one ex2.
         bool ok = mbar_wait(&bars[BAR_QK], par) && mbar_wait(&bars[BAR_G], par);
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        const int a = tid >> 6, cpair = tid & 63, c0 = 2 * cpair;
-        float gl0[16], gl1[16];
         {
-            float acc0 = 0.f, acc1 = 0.f;
-            const float* G = reinterpret_cast<const float*>(sm + OFF_G);
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const float2 gv = *reinterpret_cast<const float2*>(G + (16 * a + i) * kD + c0);
-                flags |= decay_flags(gv.x) | decay_flags(gv.y);
-                acc0 += gv.x;
-                acc1 += gv.y;
-                gl0[i] = acc0;
-                gl1[i] = acc1;
-            }
-            sgend[a * kD + c0] = acc0;
-            sgend[a * kD + c0 + 1] = acc1;
+            const int a = warp >> 2, cb = warp & 3;
+            const int j = (tid & 31) >> 2, g8 = tid & 3;
+            const int c0 = cb * 32 + g8 * 8;
             if (tid < kC) {
-                float bv = tid < L ? p.beta[((size_t)b * T + t0 + tid) * p.H + h] : 0.f;
-                flags |= finite_flag(bv);
-                sbeta[tid] = bv;
+                flags |= finite_flag(beta_next);
+                sbeta[tid] = beta_next;
             }
-        }
-        __syncthreads();
-        {
-            float ge0[4], ge1[4];
+            beta_next = load_beta(c + 1);
+            float gam[2][8];  // in-tile inclusive cumulative log2-decay, rows 2j, 2j+1
+            float mn = 0.f, mx = -5.f, sum = 0.f;
 #pragma unroll
-            for (int bb = 0; bb < 4; bb++) {
-                ge0[bb] = sgend[bb * kD + c0];
-                ge1[bb] = sgend[bb * kD + c0 + 1];
-            }
-            float pre0 = 0.f, pre1 = 0.f, post0 = 0.f, post1 = 0.f;
+            for (int e = 0; e < 2; e++) {
+                const int r = 16 * a + 2 * j + e;
+                const unsigned char* grow = sm + OFF_G + cb * 8192 + r * 128;
 #pragma unroll
-            for (int bb = 0; bb < 4; bb++) {
-                if (bb < a) { pre0 += ge0[bb]; pre1 += ge1[bb]; }
-                if (bb > a) { post0 += ge0[bb]; post1 += ge1[bb]; }
-            }
-            const float eA0 = __expf(pre0), eA1 = __expf(pre1);        // e^{G_a-}
-            const float eC0 = __expf(post0), eC1 = __expf(post1);      // e^{G_C - G_a+}
-            const float eE0 = __expf(ge0[a]), eE1 = __expf(ge1[a]);    // e^{tile total}
-            if (a == 0) {
-                slam[c0] = __expf(ge0[0] + ge0[1] + ge0[2] + ge0[3]);
-                slam[c0 + 1] = __expf(ge1[0] + ge1[1] + ge1[2] + ge1[3]);
-            }
-            // e^{G_{a'-} - G_{a+}} for the later windows a' > a
-            float R0[4], R1[4];
-            {
-                float s0 = 0.f, s1 = 0.f;
+                for (int hq = 0; hq < 2; hq++) {
+                    const int chk = (2 * g8 + hq) ^ (r & 7);
+                    const float4 v = *reinterpret_cast<const float4*>(grow + chk * 16);
+                    const float gv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int ap = 0; ap < 4; ap++) {
-                    R0[ap] = __expf(s0);
-                    R1[ap] = __expf(s1);
-                    if (ap > a) { s0 += ge0[ap]; s1 += ge1[ap]; }
+                    for (int z = 0; z < 4; z++) {
+                        mn = fminf(mn, gv[z]);
+                        mx = fmaxf(mx, gv[z]);
+                        sum += gv[z];
+                        gam[e][4 * hq + z] = gv[z] * kLog2e;
+                    }
                 }
             }
-            unsigned char* KQP = sm + OFF_KQP;
-            unsigned char* KM = sm + OFF_KM;
+            if (!(fabsf(sum) <= 3.402823466e38f)) flags |= KDA_DEV_NONFINITE;
+            else if (mn < kLogDecayMin || mx > 0.f) flags |= KDA_DEV_DECAY_RANGE;
+            // scan over the 8 row pairs of the tile (lanes g8, g8+4, ..., g8+28)
+            float tile_tot[8];
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const int r = 16 * a + i;
-                const float e10 = __expf(gl0[i]), e11 = __expf(gl1[i]);     // e^{G_r - G_a-} <= 1
-                const float em0 = __expf(-gl0[i]), em1 = __expf(-gl1[i]);  // e^{G_a- - G_r} < e^80
-                uint32_t* pk = reinterpret_cast<uint32_t*>(KQP + sw128_offset(r, c0, 128));
-                uint32_t* pq = reinterpret_cast<uint32_t*>(KQP + sw128_offset(64 + r, c0, 128));
-                const float2 kk = unpack_bf16(*pk);
-                const float2 qq = unpack_bf16(*pq);
-                const float kp0 = kk.x * e10, kp1 = kk.y * e11;
-                const float qp0 = qq.x * e10, qp1 = qq.y * e11;
-                *pk = pack_bf16(kp0, kp1);
-                *pq = pack_bf16(qp0, qp1);
-                const float ke0 = kk.x * (em0 * eE0), ke1 = kk.y * (em1 * eE1);  // k e^{G_a+ - G_r}
-                // own window: the bounded reciprocal decay (the dense-diagonal operand)
-                *reinterpret_cast<uint32_t*>(KM + sw128_offset(win_row(a) + r, c0, KM_ROWS)) =
-                    pack_bf16(kk.x * em0, kk.y * em1);
+            for (int z = 0; z < 8; z++) {
+                gam[1][z] += gam[0][z];
+                float x = gam[1][z];
 #pragma unroll
-                for (int ap = 0; ap < 4; ap++)
-                    if (ap > a)
-                        *reinterpret_cast<uint32_t*>(
-                            KM + sw128_offset(win_row(ap) + r, c0, KM_ROWS)) =
-                            pack_bf16(ke0 * R0[ap], ke1 * R1[ap]);
-                *reinterpret_cast<uint32_t*>(sm + OFF_KT + sw128_offset(r, c0, 64)) =
-                    pack_bf16(kp0 * eA0, kp1 * eA1);
-                *reinterpret_cast<uint32_t*>(sm + OFF_QT + sw128_offset(r, c0, 64)) =
-                    pack_bf16(qp0 * eA0, qp1 * eA1);
-                *reinterpret_cast<uint32_t*>(sm + OFF_KB + sw128_offset(r, c0, 64)) =
-                    pack_bf16(ke0 * eC0, ke1 * eC1);
+                for (int off = 1; off < 8; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, 4 * off);
+                    if (j >= off) x += y;
+                }
+                const float excl = x - gam[1][z];
+                gam[0][z] += excl;
+                gam[1][z] += excl;
+                tile_tot[z] = __shfl_sync(0xffffffffu, x, 28 + g8);
+            }
+            if (j == 0) {
+                *reinterpret_cast<float4*>(sgt + a * kD + c0) =
+                    make_float4(tile_tot[0], tile_tot[1], tile_tot[2], tile_tot[3]);
+                *reinterpret_cast<float4*>(sgt + a * kD + c0 + 4) =
+                    make_float4(tile_tot[4], tile_tot[5], tile_tot[6], tile_tot[7]);
+            }
+            __syncthreads();
+            // Per (tile, channel) decay constants, once, into the (now free) g buffer:
+            //   0: e^{G_a-}  1: e^{G_C - G_a+}  2: e^{tile total}  3..5: e^{G_{a'-} - G_a+}, a' = 1..3
+            float* CT = reinterpret_cast<float*>(sm + OFF_G);
+            {
+                const int ta = tid >> 7, ch = tid & 127;
+                float tb[4];
+#pragma unroll
+                for (int bb = 0; bb < 4; bb++) tb[bb] = sgt[bb * kD + ch];
+                float pre = 0.f, post = 0.f, own = 0.f;
+#pragma unroll
+                for (int bb = 0; bb < 4; bb++) {
+                    if (bb < ta) pre += tb[bb];
+                    if (bb > ta) post += tb[bb];
+                    if (bb == ta) own = tb[bb];
+                }
+                CT[(ta * 6 + 0) * kD + ch] = fast_exp2(pre);
+                CT[(ta * 6 + 1) * kD + ch] = fast_exp2(post);
+                CT[(ta * 6 + 2) * kD + ch] = fast_exp2(own);
+                float run = 0.f;
+#pragma unroll
+                for (int ap = 1; ap < 4; ap++) {
+                    CT[(ta * 6 + 2 + ap) * kD + ch] = fast_exp2(run);
+                    if (ap > ta) run += tb[ap];
+                }
+                if (ta == 0) slam[ch] = fast_exp2(tb[0] + tb[1] + tb[2] + tb[3]);
+            }
+            __syncthreads();
+            float cst[6][8];
+#pragma unroll
+            for (int k6 = 0; k6 < 6; k6++) {
+                const float4 w0 = *reinterpret_cast<const float4*>(CT + (a * 6 + k6) * kD + c0);
+                const float4 w1 = *reinterpret_cast<const float4*>(CT + (a * 6 + k6) * kD + c0 + 4);
+                cst[k6][0] = w0.x; cst[k6][1] = w0.y; cst[k6][2] = w0.z; cst[k6][3] = w0.w;
+                cst[k6][4] = w1.x; cst[k6][5] = w1.y; cst[k6][6] = w1.z; cst[k6][7] = w1.w;
+            }
+            const uint32_t blk = (uint32_t)(c0 >> 6);
+            const uint32_t chunk = (uint32_t)((c0 & 63) >> 3);
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int r = 16 * a + 2 * j + e;
+                const uint32_t ro = (uint32_t)r * 128u + ((chunk ^ (uint32_t)(r & 7)) << 4);
+                unsigned char* pk = sm + OFF_KQP + blk * 16384u + ro;
+                unsigned char* pq = pk + 8192u;
+                float kf[8], qf[8], e1[8], em[8];
+                unpack8(*reinterpret_cast<const uint4*>(pk), kf);
+                unpack8(*reinterpret_cast<const uint4*>(pq), qf);
+#pragma unroll
+                for (int z = 0; z < 8; z++) {
+                    e1[z] = fast_exp2(gam[e][z]);   // e^{G_r - G_a-} <= 1
+                    em[z] = fast_exp2(-gam[e][z]);  // e^{G_a- - G_r} < e^80
+                }
+                float kp[8], qp[8], ke[8], t8[8];
+#pragma unroll
+                for (int z = 0; z < 8; z++) {
+                    kp[z] = kf[z] * e1[z];
+                    qp[z] = qf[z] * e1[z];
+                    ke[z] = kf[z] * (em[z] * cst[2][z]);  // k e^{G_a+ - G_r}, <= |k|
+                    t8[z] = kf[z] * em[z];                // own window: bounded reciprocal decay
+                }
+                *reinterpret_cast<uint4*>(pk) = pack8(kp);
+                *reinterpret_cast<uint4*>(pq) = pack8(qp);
+                unsigned char* pw = sm + OFF_KM + blk * (KM_ROWS * 128u) + ro;
+                *reinterpret_cast<uint4*>(pw + (uint32_t)win_row(a) * 128u) = pack8(t8);
+#pragma unroll
+                for (int ap = 1; ap < 4; ap++) {
+                    if (ap > a) {
+#pragma unroll
+                        for (int z = 0; z < 8; z++) t8[z] = ke[z] * cst[2 + ap][z];
+                        *reinterpret_cast<uint4*>(pw + (uint32_t)win_row(ap) * 128u) = pack8(t8);
+                    }
+                }
+                const uint32_t o64 = blk * 8192u + ro;
+#pragma unroll
+                for (int z = 0; z < 8; z++) t8[z] = kp[z] * cst[0][z];
+                *reinterpret_cast<uint4*>(sm + OFF_KT + o64) = pack8(t8);
+#pragma unroll
+                for (int z = 0; z < 8; z++) t8[z] = qp[z] * cst[0][z];
+                *reinterpret_cast<uint4*>(sm + OFF_QT + o64) = pack8(t8);
+#pragma unroll
+                for (int z = 0; z < 8; z++) t8[z] = ke[z] * cst[1][z];
+                *reinterpret_cast<uint4*>(sm + OFF_KB + o64) = pack8(t8);
             }
         }
         fence_proxy_async_smem();
@@ -349,19 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             if (c + 1 < nchunks) issue_g(c + 1);
             tc_fence_after();
+            const uint64_t ad0 = desc_kmajor(sbase + OFF_KQP);
 #pragma unroll
             for (int ta = 0; ta < 4; ta++) {
-                const int N = 16 * (ta + 1);
-                const uint32_t idesc = idesc_bf16(128, N, 0, 0);
-                const uint32_t bwin = sbase + OFF_KM + (uint32_t)win_row(ta) * 128u;
+                const uint32_t idesc = idesc_bf16(128, 16 * (ta + 1), 0, 0);
+                const uint64_t bd0 = desc_kmajor(sbase + OFF_KM + (uint32_t)win_row(ta) * 128u);
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {
-                    const uint64_t ad = desc_kmajor(sbase + OFF_KQP, 128, kk);
-                    const uint64_t bd = sdesc_sw128(
-                        bwin + (uint32_t)(kk >> 2) * (KM_ROWS * 128u) + (uint32_t)(kk & 3) * 32u,
-                        16, 1024);
-                    mma_bf16(tbase + TM_SCR + win_row(ta), ad, bd, idesc, kk > 0);
-                }
+                for (int kk = 0; kk < 8; kk++)
+                    mma_bf16(tbase + TM_SCR + win_row(ta), ad0 + kstep_kmajor(128, kk),
+                             bd0 + kstep_kmajor(KM_ROWS, kk), idesc, kk > 0);
             }
             mma_commit(&bars[BAR_MMA]);
         }
@@ -370,24 +471,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0 && c + 1 < nchunks) issue_qk(c + 1);
 
-        // Gram readout: warps 0-3, lane = row (0..63: A, 64..127: P)
-        if (tid < 128) {
-            const int part = warp >> 1;
-            const int r = tid & 63;
-            const float beta_r = sbeta[r];
-            const uint32_t tl = tmem_at(tbase, warp * 32, 0);
-            if ((warp & 1) == 0) {  // tiles 0, 1: window columns [0, 48)
-                float v[48];
+        // Gram readout. Quarter q: rows 32(q&1).. of A (q < 2) or P (q >= 2);
+        // warp u writes output columns [16u, 16u + 16).
+        {
+            const int part = q >> 1;
+            const int r = 32 * (q & 1) + (tid & 31);
+            const int a = r >> 4, a0 = 2 * (q & 1);
+            float v0[16], v1[16];
 #pragma unroll
-                for (int j = 0; j < 48; j += 16) tmem_ld16(tl + TM_SCR + j, v + j);
-                if (r < 16) gram_rows<0, 0>(v, r, part, beta_r, sm);
-                else gram_rows<1, 16>(v, r, part, beta_r, sm);
-            } else {  // tiles 2, 3: window columns [48, 160)
-                float v[112];
+            for (int jj = 0; jj < 16; jj++) { v0[jj] = 0.f; v1[jj] = 0.f; }
+            if (u <= a0) tmem_ld16(tq + TM_SCR + win_row(a0) + 16 * u, v0);
+            if (u <= a0 + 1) tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * u, v1);
+            const bool second = (a == a0 + 1);
+            const bool live = (u <= a);
+            float out[16];
+            if (part == 0) {
+                const float br = sbeta[r];
 #pragma unroll
-                for (int j = 0; j < 112; j += 16) tmem_ld16(tl + TM_SCR + 48 + j, v + j);
-                if (r < 48) gram_rows<2, 0>(v, r, part, beta_r, sm);
-                else gram_rows<3, 48>(v, r, part, beta_r, sm);
+                for (int jj = 0; jj < 16; jj++) {
+                    const int s = 16 * u + jj;
+                    const float val = second ? v1[jj] : v0[jj];
+                    out[jj] = (live && s < r) ? br * val : 0.f;
+                }
+                float* FA = reinterpret_cast<float*>(sm + OFF_FA) + r * LDA + 16 * u;
+#pragma unroll
+                for (int jj = 0; jj < 16; jj++) FA[jj] = out[jj];
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; jj++) {
+                    const int s = 16 * u + jj;
+                    const float val = second ? v1[jj] : v0[jj];
+                    out[jj] = (live && s <= r) ? val : 0.f;
+                }
+                st_row8(sm + OFF_A0, 64 + r, 16 * u, 128, out);
+                st_row8(sm + OFF_A0, 64 + r, 16 * u + 8, 128, out + 8);
             }
         }
         tc_fence_before();
@@ -395,61 +512,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ------------------------------------------------------------ T = (I + A)^-1
         {
-            float* FA = reinterpret_cast<float*>(sm + OFF_FA);
+            const float* FA = reinterpret_cast<const float*>(sm + OFF_FA);
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
-            if (tid < 64) {  // diagonal 16x16 blocks, one column per thread
-                const int ta = tid >> 4, j = tid & 15, o0 = 16 * ta;
-                float x[16];
+            if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
+                const int o0 = 16 * warp, jc = tid & 15;
+                float acc[16], x[16];
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    float acc = 0.f;
+                for (int i = 0; i < 16; i++) acc[i] = 0.f;
 #pragma unroll
-                    for (int m = 0; m < i; m++)
-                        if (m >= j) acc += FA[(o0 + i) * LDF + o0 + m] * x[m];
-                    x[i] = (i < j) ? 0.f : (i == j ? 1.f : -acc);
+                for (int m = 0; m < 16; m++) {  // right-looking: finish x_m, push into later rows
+                    x[m] = (m < jc) ? 0.f : ((m == jc) ? 1.f : -acc[m]);
+#pragma unroll
+                    for (int i = m + 1; i < 16; i++) acc[i] += FA[(o0 + i) * LDA + o0 + m] * x[m];
                 }
+                if ((tid & 31) < 16) {
 #pragma unroll
-                for (int i = 0; i < 16; i++) FT[(o0 + i) * LDF + o0 + j] = x[i];
+                    for (int i = 0; i < 16; i++) FT[(o0 + i) * LDT + o0 + jc] = x[i];
+                }
+            } else {  // zero the six blocks above the diagonal
+                for (int e = tid - 128; e < 6 * 256; e += kThreads - 128) {
+                    const int blkid = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+                    const int br = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
+                    const int bc = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
+                    FT[(16 * br + i) * LDT + 16 * bc + jj] = 0.f;
+                }
             }
             __syncthreads();
-            // off-diagonal blocks by distance: T_ab = -T_aa sum_{c=b}^{a-1} A_ac T_cb
-            for (int dd = 1; dd < 4; dd++) {
-                const int nblk = 4 - dd;
-                for (int e = tid; e < nblk * 256; e += kThreads) {
-                    const int bb = e >> 8, i = (e >> 4) & 15, j = e & 15, aa = bb + dd;
-                    float acc = 0.f;
-                    for (int cc = bb; cc < aa; cc++)
-#pragma unroll
-                        for (int m = 0; m < 16; m++)
-                            acc += FA[(16 * aa + i) * LDF + 16 * cc + m] *
-                                   FT[(16 * cc + m) * LDF + 16 * bb + j];
-                    MS[bb * 272 + i * 17 + j] = acc;
-                }
-                __syncthreads();
-                for (int e = tid; e < nblk * 256; e += kThreads) {
-                    const int bb = e >> 8, i = (e >> 4) & 15, j = e & 15, aa = bb + dd;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; m++)
-                        acc += FT[(16 * aa + i) * LDF + 16 * aa + m] * MS[bb * 272 + m * 17 + j];
-                    FT[(16 * aa + i) * LDF + 16 * bb + j] = -acc;
-                }
-                __syncthreads();
-            }
-            // T' = T Diag(beta) -> rows 0..63 of A0 (bf16), zero above the diagonal
+            merge_block_row<1, 1>(FA, FT, MS, tid);
+            merge_block_row<2, 2>(FA, FT, MS, tid);
+            merge_block_row<3, 2>(FA, FT, MS, tid);
+            // T' = T Diag(beta) -> rows 0..63 of A0 (bf16)
             {
-                const int r = tid >> 2, s0 = (tid & 3) * 16;
+                const int r = tid >> 3, s0 = (tid & 7) * 8;
+                float x[8];
 #pragma unroll
-                for (int h8 = 0; h8 < 16; h8 += 8) {
-                    float x[8];
-#pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        const int s = s0 + h8 + j;
-                        x[j] = (s <= r) ? FT[r * LDF + s] * sbeta[s] : 0.f;
-                    }
-                    st_row8(sm + OFF_A0, r, s0 + h8, 128, x);
-                }
+                for (int jj = 0; jj < 8; jj++) x[jj] = FT[r * LDT + s0 + jj] * sbeta[s0 + jj];
+                st_row8(sm + OFF_A0, r, s0, 128, x);
             }
         }
         fence_proxy_async_smem();
@@ -459,25 +558,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
+            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);
+            const uint64_t bd0 = desc_mnmajor(sbase + OFF_A0, 128);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_SCR, desc_kmajor(sbase + OFF_A0, 128, kk),
-                         desc_mnmajor(sbase + OFF_A0, 128, kk), idesc, kk > 0);
+                mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
+                         kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (tid >= 64 && tid < 128) {  // rows 64..127 of X -> A0 rows 64..127
-            const int r = tid - 64;
-            const uint32_t tl = tmem_at(tbase, warp * 32, TM_SCR);
-#pragma unroll
-            for (int j = 0; j < 64; j += 16) {
-                float x[16];
-                tmem_ld16(tl + j, x);
-                st_row8(sm + OFF_A0, 64 + r, j, 128, x);
-                st_row8(sm + OFF_A0, 64 + r, j + 8, 128, x + 8);
-            }
+        if (q >= 2) {  // rows 64..127 of X -> A0 rows 64..127, 16 columns per warp
+            float x[16];
+            tmem_ld16(tq + TM_SCR + 16 * u, x);
+            st_row8(sm + OFF_A0, lane, 16 * u, 128, x);
+            st_row8(sm + OFF_A0, lane, 16 * u + 8, 128, x + 8);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -489,11 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);
+            const uint64_t bk0 = desc_mnmajor(sbase + OFF_KT, 64);
+            const uint64_t bv0 = desc_mnmajor(sbase + OFF_V, 64);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++) {
-                const uint64_t ad = desc_kmajor(sbase + OFF_A0, 128, kk);
-                mma_bf16(tbase + TM_SCR, ad, desc_mnmajor(sbase + OFF_KT, 64, kk), idesc, kk > 0);
-                mma_bf16(tbase + TM_D1, ad, desc_mnmajor(sbase + OFF_V, 64, kk), idesc, kk > 0);
+                const uint64_t ad = ad0 + kstep_kmajor(128, kk);
+                mma_bf16(tbase + TM_SCR, ad, bk0 + kstep_mnmajor(kk), idesc, kk > 0);
+                mma_bf16(tbase + TM_D1, ad, bv0 + kstep_mnmajor(kk), idesc, kk > 0);
             }
             mma_commit(&bars[BAR_MMA]);
         }
@@ -502,42 +601,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
 
-        if (tid < 128) {  // [W; PW] -> A1 = [-W; Qt - PW]
-            const int lane = tid;
-            const uint32_t tl = tmem_at(tbase, warp * 32, TM_SCR);
+        {
+            // [W; PW] columns [32u, 32u + 32) -> A1 = [-W; Qt - PW]
+            float x[32];
+            tmem_ld32(tq + TM_SCR + 32 * u, x);
+            if (lane < 64) {
 #pragma unroll
-            for (int j = 0; j < 128; j += 32) {
-                float x[32];
-                tmem_ld32(tl + j, x);
-                if (lane < 64) {
+                for (int e = 0; e < 32; e++) x[e] = -x[e];
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; e++) x[e] = -x[e];
-                } else {
+                for (int e = 0; e < 32; e += 8) {
+                    float qt[8];
+                    ld_row8(sm + OFF_QT, lane - 64, 32 * u + e, 64, qt);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        float qt[8];
-                        ld_row8(sm + OFF_QT, lane - 64, j + e, 64, qt);
-#pragma unroll
-                        for (int z = 0; z < 8; z++) x[e + z] = qt[z] - x[e + z];
-                    }
+                    for (int z = 0; z < 8; z++) x[e + z] = qt[z] - x[e + z];
                 }
-#pragma unroll
-                for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, j + e, 128, x + e);
             }
-        } else {  // S0 -> bf16 operand copy; S <- e^{G_C} S in TMEM
-            const int i = tid - 128;
-            const float lam = slam[i];
-            const uint32_t tl = tmem_at(tbase, (warp & 3) * 32, TM_S);
 #pragma unroll
-            for (int j = 0; j < 128; j += 16) {
-                float x[16];
-                tmem_ld16(tl + j, x);
-                st_row8(sm + OFF_S, i, j, 128, x);
-                st_row8(sm + OFF_S, i, j + 8, 128, x + 8);
+            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, 32 * u + e, 128, x + e);
+            // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM
+            float y[32];
+            tmem_ld32(tq + TM_S + 32 * u, y);
 #pragma unroll
-                for (int e = 0; e < 16; e++) x[e] *= lam;
-                tmem_st16(tl + j, x);
-            }
+            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_S, lane, 32 * u + e, 128, y + e);
+            const float lam = slam[lane];
+#pragma unroll
+            for (int e = 0; e < 32; e++) y[e] *= lam;
+            tmem_st16(tq + TM_S + 32 * u, y);
+            tmem_st16(tq + TM_S + 32 * u + 16, y + 16);
             tmem_wait_st();
         }
         fence_proxy_async_smem();
@@ -548,43 +639,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+            const uint64_t ad0 = desc_kmajor(sbase + OFF_A1);
+            const uint64_t bd0 = desc_mnmajor(sbase + OFF_S, 128);
 #pragma unroll
             for (int kk = 0; kk < 8; kk++)
-                mma_bf16(tbase + TM_D1, desc_kmajor(sbase + OFF_A1, 128, kk),
-                         desc_mnmajor(sbase + OFF_S, 128, kk), idesc, 1);
+                mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
+                         1);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         {
-            const int lane = (warp & 3) * 32 + (tid & 31);
-            const int cb = (warp >> 2) * 64;
-            const uint32_t tl = tmem_at(tbase, (warp & 3) * 32, TM_D1 + cb);
+            float x[32];
+            tmem_ld32(tq + TM_D1 + 32 * u, x);
             if (lane < 64) {  // U rows -> bf16 operand
 #pragma unroll
-                for (int j = 0; j < 64; j += 16) {
-                    float x[16];
-                    tmem_ld16(tl + j, x);
-                    st_row8(sm + OFF_U, lane, cb + j, 64, x);
-                    st_row8(sm + OFF_U, lane, cb + j + 8, 64, x + 8);
-                }
+                for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_U, lane, 32 * u + e, 64, x + e);
             } else {  // O rows -> global
                 const int r = lane - 64;
-                __nv_bfloat16* dst = p.o + (((size_t)b * T + t0 + r) * p.H + h) * kD + cb;
+                if (r < L) {
+                    __nv_bfloat16* dst = p.o + (((size_t)b * T + t0 + r) * p.H + h) * kD + 32 * u;
 #pragma unroll
-                for (int j = 0; j < 64; j += 16) {
-                    float x[16];
-                    tmem_ld16(tl + j, x);
-                    if (r < L) {
-                        uint4 u0, u1;
-                        u0.x = pack_bf16(x[0], x[1]);   u0.y = pack_bf16(x[2], x[3]);
-                        u0.z = pack_bf16(x[4], x[5]);   u0.w = pack_bf16(x[6], x[7]);
-                        u1.x = pack_bf16(x[8], x[9]);   u1.y = pack_bf16(x[10], x[11]);
-                        u1.z = pack_bf16(x[12], x[13]); u1.w = pack_bf16(x[14], x[15]);
-                        *reinterpret_cast<uint4*>(dst + j) = u0;
-                        *reinterpret_cast<uint4*>(dst + j + 8) = u1;
-                    }
+                    for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
                 }
             }
         }
@@ -596,10 +673,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 128, 1, 1);
+            const uint64_t ad0 = desc_mnmajor(sbase + OFF_KB, 64);
+            const uint64_t bd0 = desc_mnmajor(sbase + OFF_U, 64);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_S, desc_mnmajor(sbase + OFF_KB, 64, kk),
-                         desc_mnmajor(sbase + OFF_U, 64, kk), idesc, 1);
+                mma_bf16(tbase + TM_S, ad0 + kstep_mnmajor(kk), bd0 + kstep_mnmajor(kk), idesc, 1);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
@@ -610,17 +688,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // Final state -> hT.
     if (p.hT && !failed) {
-        const int lane = (warp & 3) * 32 + (tid & 31);
-        const int cbase = (warp >> 2) * 64;
-        float* dst = p.hT + ((size_t)blockIdx.x * kD + lane) * kD + cbase;
-        const uint32_t tl = tmem_at(tbase, (warp & 3) * 32, TM_S + cbase);
+        float* dst = p.hT + ((size_t)blockIdx.x * kD + lane) * kD + 32 * u;
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 16) {
+        for (int cc = 0; cc < 32; cc += 16) {
             float x[16];
-            tmem_ld16(tl + cc, x);
+            tmem_ld16(tq + TM_S + 32 * u + cc, x);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(dst + cc + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+            for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(dst + cc + jj) =
+                    make_float4(x[jj], x[jj + 1], x[jj + 2], x[jj + 3]);
         }
     }
     report_flags(p.d_status, flags);
@@ -634,18 +710,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
+        cudaDriverEntryPointQueryResult qr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     }
     return fn;
 }
 
-// 4-D map over [B, T, H, d] (innermost first: d, H, T, B).
+// 4-D map over [B, T, H, d] (innermost first: d, H, T, B), boxes of
+// box_inner x 1 x 64 x 1 with the 128-byte swizzle. Rows past T read as zero.
 bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, int B, int T,
-              int H, int d, int box_inner, CUtensorMapSwizzle swz) {
+              int H, int d, int box_inner) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -654,8 +731,8 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, 
     cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, (cuuint32_t)kC, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -666,14 +743,10 @@ cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
     CUtensorMap mq{}, mk{}, mv{}, mg{};
     if (a.T > 0) {
         const int T = a.T;
-        if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, T, a.H, kD, kD,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64) ||
+            !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64) ||
+            !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64) ||
+            !make_map(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, T, a.H, kD, 32))
             return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel,
