@@ -202,9 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
                         const __grid_constant__ CUtensorMap map_g, const TcParams p) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // Align to 1024 bytes (the 128-byte swizzle atom) by offsetting the
+    // __shared__ array itself, so every access below stays an LDS/STS: an
+    // integer round trip would turn them into generic loads and stores.
+    unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t bars[NBAR];
     __shared__ uint32_t tmem_slot;
 
