@@ -18,9 +18,9 @@
 //   T' = (I + A)^-1 Diag(b),  Kt = k e^{G},  Qt = q e^{G},  Kb = k e^{G_C - G}
 //   W = T' Kt,  Ut = T' V,  U = Ut - W S0,  O = Qt S0 + P U,  S_C = Diag(e^{G_C}) S0 + Kb^T U.
 // Rewritten for 128-row MMAs with X = P T':
-//   round 1  Gram blocks  [Kp; Qp] * Km_a^T                  (4 MMAs, N = 16(a+1))
+//   round 1  Gram blocks  [Kp; Qp] * [Km_0; Km_1; Km_2; Km_3]^T   (N = 16+32+48+64)
 //   round 2  X      = [T'; P] * T'          (rows 64..127 used)
-//   round 3  [W; PW]   = [T'; X] * Kt,   [Ut; P Ut] = [T'; X] * V   (the latter into D1)
+//   round 3  [Ut; P Ut | W; PW] = [T'; X] * [V | Kt]   (N = 256: D1, then scratch)
 //   round 4  D1    += [-W; Qt - PW] * S0   ->  D1 = [U; O]
 //   round 5  S     += Kb^T * U              (S pre-scaled by e^{G_C} in TMEM)
 //
@@ -69,7 +69,7 @@ constexpr int LDT = 68;  // fp32 T: 16-byte rows for float4 strips
 constexpr int LDM = 52;
 constexpr uint32_t OFF_FA = OFF_KM;           // fp32 A [64][65]
 constexpr uint32_t OFF_FT = OFF_KM + 16640;   // fp32 T [64][68]
-constexpr uint32_t OFF_MS = OFF_KM + 34048;   // fp32 2 x [16][52] block-row partial products
+constexpr uint32_t OFF_MS = OFF_KM + 34048;   // fp32 [16][52] block-row product
 constexpr uint32_t OFF_A1 = OFF_KM;           // [-W; Q'], SW128 128 x 128
 constexpr uint32_t OFF_S = OFF_KT;            // S0 bf16, SW128 128 x 128 (MN-major B)
 constexpr int KM_ROWS = 160;                  // windows of 16, 32, 48, 64 rows
@@ -144,55 +144,74 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int R) {
 }
 __device__ __forceinline__ uint64_t kstep_mnmajor(int kk) { return (uint64_t)(kk * 128); }
 
+// Warp-level TF32 MMA (m16n8k8, fp32 accumulate) for the 16-row blocks of
+// the triangular inverse: tcgen05 needs M >= 64, these products are 16 x 16.
+// Fragment ownership (g = lane / 4, t = lane % 4): A rows g, g+8 and columns
+// t, t+4; B rows t, t+4 and column g; D rows g, g+8 and columns 2t, 2t+1.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // One block row of the blocked triangular inverse T = (I + A)^-1 (AB = 1..3):
 // with the diagonal blocks and block rows < AB known,
-//   M         = A[AB, <AB] T[<AB, <AB]    (16 x 16AB; K split in KS parts)
+//   M         = A[AB, <AB] T[<AB, <AB]    (16 x 16AB)
 //   T[AB,<AB] = -T[AB, AB] M
-// T is stored with zeros above the diagonal, so every loop has a compile-time
-// trip count and no predicate.
-template <int AB, int KS>
-__device__ __forceinline__ void merge_block_row(const float* FA, float* FT, float* MS, int tid) {
-    constexpr int RB = 16 * AB, NS = 4 * RB, KL = RB / KS;
-    if (tid < NS * KS) {
-        const int part = tid / NS, strip = tid % NS;
-        const int i = strip / (RB / 4), s0 = 4 * (strip % (RB / 4));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* arow = FA + (RB + i) * LDA + part * KL;
-        const float* tcol = FT + part * KL * LDT + s0;
+// Warp w < 2AB owns the 8 output columns 8w..8w+7. T is stored with zeros
+// above the diagonal, so the K loop starts at that column block.
+template <int AB>
+__device__ __forceinline__ void merge_block_row(const float* FA, float* FT, float* MS, int warp,
+                                                int lane) {
+    constexpr int RB = 16 * AB;
+    const int g = lane >> 2, t = lane & 3;
+    if (warp < 2 * AB) {
+        const int n0 = 8 * warp;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* ar0 = FA + (RB + g) * LDA;
+        const float* ar1 = FA + (RB + g + 8) * LDA;
 #pragma unroll
-        for (int m = 0; m < KL; m++) {
-            const float av = arow[m];
-            const float4 tv = *reinterpret_cast<const float4*>(tcol + m * LDT);
-            acc.x += av * tv.x;
-            acc.y += av * tv.y;
-            acc.z += av * tv.z;
-            acc.w += av * tv.w;
+        for (int ks = 0; ks < 2 * AB; ks++) {
+            if (ks >= 2 * (warp >> 1)) {  // T[k, n] = 0 for k above n's 16-column block
+                const int k0 = 8 * ks;
+                const uint32_t af[4] = {to_tf32(ar0[k0 + t]), to_tf32(ar1[k0 + t]),
+                                        to_tf32(ar0[k0 + t + 4]), to_tf32(ar1[k0 + t + 4])};
+                const uint32_t bf[2] = {to_tf32(FT[(k0 + t) * LDT + n0 + g]),
+                                        to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
+                mma_tf32(acc, af, bf);
+            }
         }
-        *reinterpret_cast<float4*>(MS + part * 16 * LDM + i * LDM + s0) = acc;
+        MS[g * LDM + n0 + 2 * t] = acc[0];
+        MS[g * LDM + n0 + 2 * t + 1] = acc[1];
+        MS[(g + 8) * LDM + n0 + 2 * t] = acc[2];
+        MS[(g + 8) * LDM + n0 + 2 * t + 1] = acc[3];
     }
     __syncthreads();
-    if (tid < NS) {
-        const int i = tid / (RB / 4), s0 = 4 * (tid % (RB / 4));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* trow = FT + (RB + i) * LDT + RB;
+    if (warp < 2 * AB) {
+        const int n0 = 8 * warp;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* tr0 = FT + (RB + g) * LDT + RB;
+        const float* tr1 = FT + (RB + g + 8) * LDT + RB;
 #pragma unroll
-        for (int m = 0; m < 16; m++) {
-            const float tv = trow[m];
-            float4 mv = *reinterpret_cast<const float4*>(MS + m * LDM + s0);
-            if (KS > 1) {
-                const float4 m2 = *reinterpret_cast<const float4*>(MS + 16 * LDM + m * LDM + s0);
-                mv.x += m2.x;
-                mv.y += m2.y;
-                mv.z += m2.z;
-                mv.w += m2.w;
-            }
-            acc.x += tv * mv.x;
-            acc.y += tv * mv.y;
-            acc.z += tv * mv.z;
-            acc.w += tv * mv.w;
+        for (int ks = 0; ks < 2; ks++) {
+            const int k0 = 8 * ks;
+            const uint32_t af[4] = {to_tf32(tr0[k0 + t]), to_tf32(tr1[k0 + t]),
+                                    to_tf32(tr0[k0 + t + 4]), to_tf32(tr1[k0 + t + 4])};
+            const uint32_t bf[2] = {to_tf32(MS[(k0 + t) * LDM + n0 + g]),
+                                    to_tf32(MS[(k0 + t + 4) * LDM + n0 + g])};
+            mma_tf32(acc, af, bf);
         }
-        *reinterpret_cast<float4*>(FT + (RB + i) * LDT + s0) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        FT[(RB + g) * LDT + n0 + 2 * t] = -acc[0];
+        FT[(RB + g) * LDT + n0 + 2 * t + 1] = -acc[1];
+        FT[(RB + g + 8) * LDT + n0 + 2 * t] = -acc[2];
+        FT[(RB + g + 8) * LDT + n0 + 2 * t + 1] = -acc[3];
     }
     __syncthreads();
 }
@@ -456,16 +475,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             if (c + 1 < nchunks) issue_g(c + 1);
             tc_fence_after();
+            // The four windows are consecutive rows of one tile, so a single
+            // N = 160 product computes every Gram block: columns win_row(a)..
+            // of D hold the block anchored at tile a.
             const uint64_t ad0 = desc_kmajor(sbase + OFF_KQP);
+            const uint64_t bd0 = desc_kmajor(sbase + OFF_KM);
+            const uint32_t idesc = idesc_bf16(128, KM_ROWS, 0, 0);
 #pragma unroll
-            for (int ta = 0; ta < 4; ta++) {
-                const uint32_t idesc = idesc_bf16(128, 16 * (ta + 1), 0, 0);
-                const uint64_t bd0 = desc_kmajor(sbase + OFF_KM + (uint32_t)win_row(ta) * 128u);
-#pragma unroll
-                for (int kk = 0; kk < 8; kk++)
-                    mma_bf16(tbase + TM_SCR + win_row(ta), ad0 + kstep_kmajor(128, kk),
-                             bd0 + kstep_kmajor(KM_ROWS, kk), idesc, kk > 0);
-            }
+            for (int kk = 0; kk < 8; kk++)
+                mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_kmajor(KM_ROWS, kk),
+                         idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
@@ -541,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncthreads();
-            merge_block_row<1, 1>(FA, FT, MS, tid);
-            merge_block_row<2, 2>(FA, FT, MS, tid);
-            merge_block_row<3, 2>(FA, FT, MS, tid);
+            merge_block_row<1>(FA, FT, MS, warp, tid & 31);
+            merge_block_row<2>(FA, FT, MS, warp, tid & 31);
+            merge_block_row<3>(FA, FT, MS, warp, tid & 31);
             // T' = T Diag(beta) -> rows 0..63 of A0 (bf16)
             {
                 const int r = tid >> 3, s0 = (tid & 7) * 8;
@@ -586,16 +605,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+            // v and Kt are adjacent 64-row tiles, i.e. one MN-major operand of
+            // N = 256 whose first half lands in D1 ([Ut; P Ut]) and second half
+            // in the scratch columns ([W; PW]).
+            static_assert(OFF_KT == OFF_V + 16384 && TM_SCR == TM_D1 + 128, "round-3 fusion layout");
+            const uint32_t idesc = idesc_bf16(128, 256, 0, 1);
             const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);
-            const uint64_t bk0 = desc_mnmajor(sbase + OFF_KT, 64);
-            const uint64_t bv0 = desc_mnmajor(sbase + OFF_V, 64);
+            const uint64_t bd0 = desc_mnmajor(sbase + OFF_V, 64);
 #pragma unroll
-            for (int kk = 0; kk < 4; kk++) {
-                const uint64_t ad = ad0 + kstep_kmajor(128, kk);
-                mma_bf16(tbase + TM_SCR, ad, bk0 + kstep_mnmajor(kk), idesc, kk > 0);
-                mma_bf16(tbase + TM_D1, ad, bv0 + kstep_mnmajor(kk), idesc, kk > 0);
-            }
+            for (int kk = 0; kk < 4; kk++)
+                mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
+                         kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
