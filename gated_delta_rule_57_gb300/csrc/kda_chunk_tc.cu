@@ -165,11 +165,12 @@ __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint
 // with the diagonal blocks and block rows < AB known,
 //   M         = A[AB, <AB] T[<AB, <AB]    (16 x 16AB)
 //   T[AB,<AB] = -T[AB, AB] M
-// Warp w < 2AB owns the 8 output columns 8w..8w+7. T is stored with zeros
-// above the diagonal, so the K loop starts at that column block.
+// Warp w < 2AB owns the 8 output columns 8w..8w+7. Blocks of T above the
+// diagonal are never read (the K loop starts at the output's column block);
+// the finished block row also goes out as T' = T Diag(beta) in bf16.
 template <int AB>
 __device__ __forceinline__ void merge_block_row(const float* FA, float* FT, float* MS, int warp,
-                                                int lane) {
+                                                int lane, unsigned char* A0, const float* sbeta) {
     constexpr int RB = 16 * AB;
     const int g = lane >> 2, t = lane & 3;
     if (warp < 2 * AB) {
@@ -212,6 +213,12 @@ __device__ __forceinline__ void merge_block_row(const float* FA, float* FT, floa
         FT[(RB + g) * LDT + n0 + 2 * t + 1] = -acc[1];
         FT[(RB + g + 8) * LDT + n0 + 2 * t] = -acc[2];
         FT[(RB + g + 8) * LDT + n0 + 2 * t + 1] = -acc[3];
+        // T' = T Diag(beta), straight into the bf16 MMA operand
+        const float b0 = sbeta[n0 + 2 * t], b1 = sbeta[n0 + 2 * t + 1];
+        *reinterpret_cast<uint32_t*>(A0 + sw128_offset(RB + g, n0 + 2 * t, 128)) =
+            pack_bf16(-acc[0] * b0, -acc[1] * b1);
+        *reinterpret_cast<uint32_t*>(A0 + sw128_offset(RB + g + 8, n0 + 2 * t, 128)) =
+            pack_bf16(-acc[2] * b0, -acc[3] * b1);
     }
     __syncthreads();
 }
@@ -326,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int L = min(kC, T - t0);
         const uint32_t par = (uint32_t)(c & 1);
 
+        uint4 stash[2][3];
+        uint32_t p1_ro[2], p1_off;
         // ------------------------------------------------------------ P1
         // Warp = (tile a, 32-channel block cb); lane = (row pair j, 8-channel
         // group). Log-decays are kept in log2 units: each exponential is one ex2.
@@ -422,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t blk = (uint32_t)(c0 >> 6);
             const uint32_t chunk = (uint32_t)((c0 & 63) >> 3);
+            p1_off = blk * 8192u;
 #pragma unroll
             for (int e = 0; e < 2; e++) {
                 const int r = 16 * a + 2 * j + e;
@@ -456,16 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4*>(pw + (uint32_t)win_row(ap) * 128u) = pack8(t8);
                     }
                 }
-                const uint32_t o64 = blk * 8192u + ro;
+                // Kt, Qt, Kb are not read by round 1: keep them (already
+                // rounded to bf16) and store them while round 1 runs.
+                p1_ro[e] = ro;
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = kp[z] * cst[0][z];
-                *reinterpret_cast<uint4*>(sm + OFF_KT + o64) = pack8(t8);
+                stash[e][0] = pack8(t8);
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = qp[z] * cst[0][z];
-                *reinterpret_cast<uint4*>(sm + OFF_QT + o64) = pack8(t8);
+                stash[e][1] = pack8(t8);
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = ke[z] * cst[1][z];
-                *reinterpret_cast<uint4*>(sm + OFF_KB + o64) = pack8(t8);
+                stash[e][2] = pack8(t8);
             }
         }
         fence_proxy_async_smem();
@@ -486,6 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_kmajor(KM_ROWS, kk),
                          idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            *reinterpret_cast<uint4*>(sm + OFF_KT + p1_off + p1_ro[e]) = stash[e][0];
+            *reinterpret_cast<uint4*>(sm + OFF_QT + p1_off + p1_ro[e]) = stash[e][1];
+            *reinterpret_cast<uint4*>(sm + OFF_KB + p1_off + p1_ro[e]) = stash[e][2];
         }
         ok = mma_wait();
         tc_fence_after();
@@ -548,29 +566,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = m + 1; i < 16; i++) acc[i] += FA[(o0 + i) * LDA + o0 + m] * x[m];
                 }
                 if ((tid & 31) < 16) {
+                    const float bj = sbeta[o0 + jc];
 #pragma unroll
-                    for (int i = 0; i < 16; i++) FT[(o0 + i) * LDT + o0 + jc] = x[i];
+                    for (int i = 0; i < 16; i++) {
+                        FT[(o0 + i) * LDT + o0 + jc] = x[i];
+                        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_A0 + sw128_offset(o0 + i, o0 + jc, 128)) =
+                            __float2bfloat16_rn(x[i] * bj);
+                    }
                 }
-            } else {  // zero the six blocks above the diagonal
-                for (int e = tid - 128; e < 6 * 256; e += kThreads - 128) {
-                    const int blkid = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+            } else {  // T' is zero in the six blocks above the diagonal
+                for (int e = tid - 128; e < 6 * 128; e += kThreads - 128) {
+                    const int blkid = e >> 7, i = (e >> 3) & 15, jp = e & 7;
                     const int br = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
                     const int bc = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-                    FT[(16 * br + i) * LDT + 16 * bc + jj] = 0.f;
+                    *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) = 0u;
                 }
             }
             __syncthreads();
-            merge_block_row<1>(FA, FT, MS, warp, tid & 31);
-            merge_block_row<2>(FA, FT, MS, warp, tid & 31);
-            merge_block_row<3>(FA, FT, MS, warp, tid & 31);
-            // T' = T Diag(beta) -> rows 0..63 of A0 (bf16)
-            {
-                const int r = tid >> 3, s0 = (tid & 7) * 8;
-                float x[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; jj++) x[jj] = FT[r * LDT + s0 + jj] * sbeta[s0 + jj];
-                st_row8(sm + OFF_A0, r, s0, 128, x);
-            }
+            merge_block_row<1>(FA, FT, MS, warp, tid & 31, sm + OFF_A0, sbeta);
+            merge_block_row<2>(FA, FT, MS, warp, tid & 31, sm + OFF_A0, sbeta);
+            merge_block_row<3>(FA, FT, MS, warp, tid & 31, sm + OFF_A0, sbeta);
         }
         fence_proxy_async_smem();
         __syncthreads();
