@@ -283,6 +283,47 @@ def time_decode(device, seed, warmup=10):
     return total / w.steps, statistics.mean(per), w.steps
 
 
+def spec_bytes(w, K):
+    """Algorithmic bytes of one verify (state read, K tokens in, K outputs) plus
+    one commit of all K tokens (state read and written, K tokens in)."""
+    nh = w.N * w.H
+    esz = 2 if w.io == "bf16" else 4
+    state = w.dk * w.dv * 4
+    tok_in = esz * (2 * w.dk + w.dv) + 4 * w.dk + 4
+    verify = nh * (state + K * (tok_in + esz * w.dv))
+    commit = nh * (2 * state + K * tok_in)
+    return verify + commit
+
+
+def time_spec_decode(device, seed, K=4, iters=50, warmup=5):
+    """Speculative decoding round: verify K draft tokens, then commit them all."""
+    from gated_delta_rule_57_gb300 import kda
+    w = DECODE
+    x = inputs.prefill_inputs(
+        inputs.PrefillWorkload("draft", w.N, K, w.H, w.dk, w.dv, w.io, seed, h0_std=w.S_std),
+        device)
+    S = x["h0"]
+    o = torch.empty_like(x["v"])
+    stream = torch.cuda.current_stream()
+
+    def rnd():
+        kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, o=o, stream=stream)
+        kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, commit=True,
+                             want_o=False, stream=stream)
+
+    for _ in range(warmup):
+        rnd()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        rnd()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters, iters * 2
+
+
 def oracle_sample(budget_s, max_b=None):
     """Oracle on whole batch rows of the prefill workload until ~budget_s."""
     import oracle
@@ -336,6 +377,10 @@ def run_ours(args):
     dec_ach = dec_bytes / (dec_launch_ms * 1e-3) / 1e9
     dec_traffic = recorded_traffic("decode")
 
+    spec_ms, spec_launches = time_spec_decode(device, rank_seed(DECODE.seed + 1, rank))
+    spec_b = spec_bytes(DECODE, 4)
+    spec_gbs = job_value(spec_b, max_over_ranks(spec_ms, world, device), world) / 1e9
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -375,6 +420,14 @@ def run_ours(args):
                                     "algorithmic_bytes_per_launch": dec_bytes},
                        "gpu_launches": dec_steps,
                        "l2": f"state larger than L2 ({dec_bytes / 1e9:.2f} GB per step)"},
+            "spec_decode": {"workload": DECODE.name + ", 4 draft tokens",
+                            "round": "verify 4 tokens (state read) + commit 4 tokens (state "
+                                     "read and written in place)",
+                            "ms_per_round": spec_ms, "value": spec_gbs, "unit": "GB/s",
+                            "frac_of_peak_hbm": spec_gbs / peaks["hbm_gbs"],
+                            "algorithmic_bytes_per_round": spec_b,
+                            "tokens_per_s": world * DECODE.N * 4 / (spec_ms * 1e-3),
+                            "gpu_launches": spec_launches},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

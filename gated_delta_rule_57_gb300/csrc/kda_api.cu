@@ -161,4 +161,44 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
     return KDA_OK;
 }
 
+kda_status_t kda_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* S, void* o, const int* ntok, int N, int K,
+                              int H, int dk, int dv, kda_dtype_t io, int commit, int* d_status,
+                              void* stream) {
+    if (N < 0 || H < 0 || K < 0) return fail(KDA_ERR_INVALID_ARG, "N, K and H must be >= 0");
+    kda_status_t st = check_dims(dk, dv, io);
+    if (st != KDA_OK) return st;
+    if ((long long)N * H >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "N*H too large");
+    if (N == 0 || H == 0 || K == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !S)
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta and S must be non-NULL");
+    if (!o && !commit) return fail(KDA_ERR_INVALID_ARG, "verify (commit = 0) needs o");
+    const void* ptrs[] = {q, k, v, g, S, o};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (!aligned4(beta) || (ntok && !aligned4(ntok)))
+        return fail(KDA_ERR_INVALID_ARG, "beta and ntok must be 4-byte aligned");
+    const size_t esz = io == KDA_BF16 ? 2 : 4;
+    size_t n_k, n_v, n_b, n_s;
+    if (!mul_ok(&n_k, N, K, H, dk) || !mul_ok(&n_v, N, K, H, dv) || !mul_ok(&n_b, N, K, H) ||
+        !mul_ok(&n_s, N, H, dk, dv))
+        return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+    const void* ins[] = {q, k, v, g, beta, ntok};
+    const size_t in_bytes[] = {n_k * esz, n_k * esz, n_v * esz, n_k * 4, n_b * 4,
+                               ntok ? (size_t)N * 4 : 0};
+    for (int i = 0; i < 6; i++) {
+        if (overlaps(o, n_v * esz, ins[i], in_bytes[i]) || overlaps(S, n_s * 4, ins[i], in_bytes[i]))
+            return fail(KDA_ERR_INVALID_ARG, "o or S overlaps an input");
+    }
+    if (overlaps(o, n_v * esz, S, n_s * 4)) return fail(KDA_ERR_INVALID_ARG, "o overlaps S");
+    kda::MultiDecodeArgs a{q, k, v, g, beta, S, o, ntok, N, K, H, dk, dv, commit ? 1 : 0,
+                           d_status, static_cast<cudaStream_t>(stream)};
+    cudaError_t e = kda::launch_decode_multi(a, io);
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 }  // extern "C"

@@ -39,10 +39,26 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+struct MultiDecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    float* S;
+    void* o;          // may be null when commit != 0
+    const int* ntok;  // may be null: every sequence takes all K tokens
+    int N, K, H, dk, dv;
+    int commit;
+    int* d_status;
+    cudaStream_t stream;
+};
+
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_chunk_fwd_simt(const ChunkFwdArgs& a, kda_dtype_t io);
 cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a, kda_dtype_t io);
+cudaError_t launch_decode_multi(const MultiDecodeArgs& a, kda_dtype_t io);
 
 // ---------------------------------------------------------------------------
 // Device helpers

@@ -78,6 +78,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_chunk_fwd.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
             L.kda_decode_step.restype = I
+            L.kda_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I,
+                                           vp, vp]
+            L.kda_decode_multi.restype = I
             _lib = L
     return _lib
 
@@ -157,5 +160,31 @@ def kda_decode_step(q, k, v, g, beta, S, *, o=None, status: Optional[torch.Tenso
         o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
     code = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S),
                                  _ptr(o), N, H, dk, dv, io, _ptr(status), _stream(stream))
+    _check(code)
+    return o
+
+
+def kda_decode_multi(q, k, v, g, beta, S, *, ntok: Optional[torch.Tensor] = None,
+                     commit: bool = False, o=None, want_o: bool = True,
+                     status: Optional[torch.Tensor] = None, stream=None):
+    """K cached tokens per sequence in one pass (speculative decoding).
+
+    q, k, g: [N,K,H,dk]; v: [N,K,H,dv]; beta: [N,K,H]; S: [N,H,dk,dv] fp32.
+    commit=False (verify): returns o [N,K,H,dv]; S is not modified.
+    commit=True: S is advanced in place by ntok[n] tokens (int32 CUDA tensor
+    [N], or all K when None); o is returned when want_o.
+    """
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if ntok is not None and (ntok.dtype != torch.int32 or ntok.numel() != N):
+        raise ValueError("ntok must be an int32 tensor with N entries")
+    if o is None and (want_o or not commit):
+        o = torch.empty((N, K, H, dv), dtype=q.dtype, device=q.device)
+    code = lib().kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S),
+                                  _ptr(o), _ptr(ntok), N, K, H, dk, dv, io, int(bool(commit)),
+                                  _ptr(status), _stream(stream))
     _check(code)
     return o

@@ -137,6 +137,32 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
                              const float* beta, float* S, void* o, int N, int H, int dk,
                              int dv, kda_dtype_t io, int* d_status, void* stream);
 
+/*
+ * Multi-token decode for speculative decoding: K cached tokens per sequence
+ * applied to the state in one pass (section "The bill arrives in the serving
+ * stack", third bullet: the state is overwritten in place, so a rejected draft
+ * cannot be rolled back; the small projected inputs of the draft are cached
+ * and the state is rebuilt on chip instead).
+ *
+ *   q, k, g : [N, K, H, dk] (q, k of type io; g fp32)
+ *   v       : [N, K, H, dv] of type io;  beta : [N, K, H] fp32
+ *   S       : [N, H, dk, dv] fp32, the state before token 0
+ *   o       : [N, K, H, dv] of type io, o[n, t] = S_t^T q_t (tokens t < ntok[n])
+ *   ntok    : device int[N] or NULL; sequence n takes its first
+ *             min(max(ntok[n], 0), K) tokens (NULL: all K)
+ *   commit  : 0 = verify: S is only read, o is written (o must not be NULL);
+ *             1 = commit: S is overwritten with the state after ntok[n]
+ *                 tokens; o is written when not NULL
+ *
+ * Typical use: verify the K draft tokens (commit = 0), accept m_n of them,
+ * then commit with ntok = m (o = NULL). Each call reads the state once and
+ * writes it at most once. Errors and d_status as for kda_decode_step.
+ */
+kda_status_t kda_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* S, void* o, const int* ntok, int N, int K,
+                              int H, int dk, int dv, kda_dtype_t io, int commit, int* d_status,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ def L():
 
 def test_exports_every_header_symbol(L):
     names = kda.header_functions()
-    assert {"kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+    assert {"kda_chunk_fwd", "kda_decode_step", "kda_decode_multi", "kda_chunk_fwd_workspace_size",
             "kda_status_string", "kda_abi_version", "kda_last_error_string"} <= set(names)
     for n in names:
         assert hasattr(L, n), f"libkda.so does not export {n}"
@@ -106,3 +106,25 @@ def call_dec(L, q=A[0], k=A[1], v=A[2], g=A[3], beta=A[4], S=A[5], o=A[6], N=2, 
 ])
 def test_decode_rejects(L, kw, code):
     assert call_dec(L, **kw) == code
+
+
+def call_multi(L, q=A[0], k=A[1], v=A[2], g=A[3], beta=A[4], S=A[5], o=A[6], ntok=None, N=2,
+               K=4, H=1, dk=128, dv=128, io=kda.KDA_BF16, commit=0):
+    return L.kda_decode_multi(q, k, v, g, beta, S, o, ntok, N, K, H, dk, dv, io, commit, None,
+                              None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=-1), ST.KDA_ERR_INVALID_ARG),
+    (dict(o=None), ST.KDA_ERR_INVALID_ARG),          # verify needs o
+    (dict(dk=128, dv=64), ST.KDA_ERR_UNSUPPORTED),
+    (dict(ntok=A[7] + 2), ST.KDA_ERR_INVALID_ARG),   # misaligned ntok
+    (dict(S=A[2]), ST.KDA_ERR_INVALID_ARG),          # S aliases v
+    (dict(q=None), ST.KDA_ERR_INVALID_ARG),
+])
+def test_decode_multi_rejects(L, kw, code):
+    assert call_multi(L, **kw) == code
+
+
+def test_decode_multi_empty_is_a_no_op(L):
+    assert call_multi(L, K=0, q=None) == ST.KDA_OK

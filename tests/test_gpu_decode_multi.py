@@ -1,0 +1,92 @@
+"""Multi-token decode (speculative verify / commit) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_57_gb300 import inputs, kda
+from helpers import assert_o, assert_s
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def draft(N, K, H, d, io, seed):
+    """K draft tokens per sequence ([N, K, H, d] = the prefill layout) and a state."""
+    w = inputs.PrefillWorkload("draft", N, K, H, d, d, io, seed, h0_std=0.02)
+    x = inputs.prefill_inputs(w, DEV)
+    return x
+
+
+@pytest.mark.parametrize("io,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])
+def test_verify_matches_oracle_and_keeps_state(io, d):
+    x = draft(6, 5, 3, d, io, 21)
+    S = x["h0"].clone()
+    o = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S)
+    torch.cuda.synchronize()
+    assert torch.equal(S, x["h0"])  # verify never writes the state
+    xc = {n: t.cpu() for n, t in x.items()}
+    o_ref, _ = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, inputs.io_dtype(io))
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_commit_accepted_prefix(io):
+    """Per-sequence accepted lengths 0..K rebuild the state of that prefix."""
+    N, K, H, d = 6, 5, 2, 128
+    x = draft(N, K, H, d, io, 22)
+    ntok = torch.tensor([0, 1, 2, 3, 5, 9], dtype=torch.int32, device=DEV)  # 9 clamps to K
+    S = x["h0"].clone()
+    kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, ntok=ntok, commit=True,
+                         want_o=False)
+    torch.cuda.synchronize()
+    xc = {n: t.cpu() for n, t in x.items()}
+    for n, m in enumerate([0, 1, 2, 3, 5, 5]):
+        sl = slice(n, n + 1)
+        if m == 0:
+            assert torch.equal(S[n], x["h0"][n])
+            continue
+        _, h_ref = oracle.prefill(xc["q"][sl, :m], xc["k"][sl, :m], xc["v"][sl, :m],
+                                  xc["g"][sl, :m], xc["beta"][sl, :m], xc["h0"][sl])
+        assert_s(S[sl], h_ref, inputs.io_dtype(io), f"state after {m} accepted tokens")
+
+
+def test_commit_all_equals_single_steps():
+    N, K, H, d = 4, 4, 3, 128
+    x = draft(N, K, H, d, "bf16", 23)
+    S_multi = x["h0"].clone()
+    o_multi = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S_multi,
+                                   commit=True)
+    S_step = x["h0"].clone()
+    o_step = torch.stack([kda.kda_decode_step(x["q"][:, t].contiguous(), x["k"][:, t].contiguous(),
+                                              x["v"][:, t].contiguous(), x["g"][:, t].contiguous(),
+                                              x["beta"][:, t].contiguous(), S_step)
+                          for t in range(K)], dim=1)
+    torch.cuda.synchronize()
+    assert (o_multi.float() - o_step.float()).abs().max() <= 1e-2 * o_step.float().abs().max()
+    assert torch.allclose(S_multi, S_step, rtol=1e-4, atol=1e-6)
+
+
+def test_workload_n256_k4():
+    """The 256 x 32-head decode workload with 4 draft tokens: verify then commit."""
+    x = draft(256, 4, 32, 128, "bf16", 24)
+    S = x["h0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, status=status)
+    kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, commit=True,
+                         want_o=False, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    xc = {n: t.cpu() for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, torch.bfloat16)
+    assert_s(S, h_ref, torch.bfloat16)
+
+
+def test_multi_status_flags():
+    x = draft(2, 3, 2, 128, "bf16", 25)
+    x["g"][1, 2, 0, 7] = -9.0
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & kda.KDA_DEV_DECAY_RANGE
