@@ -79,12 +79,14 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
     return 0;  // both prefill paths keep their intermediates on chip
 }
 
-kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                           const float* beta, const float* h0, void* o, float* hT, int B,
-                           int T, int H, int dk, int dv, kda_dtype_t io, void* workspace,
-                           size_t ws_bytes, int* d_status, void* stream) {
-    (void)workspace;
-    (void)ws_bytes;
+}  // extern "C"
+
+namespace {
+
+kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B,
+                            int T, int H, int dk, int dv, kda_dtype_t io, float* ckpt,
+                            int ckpt_every, int* d_status, void* stream) {
     if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
@@ -114,9 +116,25 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const fl
     if (h0 && hT && h0 != hT && overlaps(hT, n_s * 4, h0, n_s * 4))
         return fail(KDA_ERR_INVALID_ARG, "hT partially overlaps h0");
     if (overlaps(o, n_v * esz, hT, n_s * 4)) return fail(KDA_ERR_INVALID_ARG, "o overlaps hT");
+    if (ckpt) {
+        if (ckpt_every <= 0 || ckpt_every % 64 != 0)
+            return fail(KDA_ERR_INVALID_ARG, "ckpt_every must be a positive multiple of 64");
+        if (!aligned16(ckpt)) return fail(KDA_ERR_INVALID_ARG, "ckpt must be 16-byte aligned");
+        size_t n_c;
+        if (!mul_ok(&n_c, n_s, (size_t)(T / ckpt_every)))
+            return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+        const void* all[] = {q, k, v, g, beta, h0, o, hT};
+        const size_t all_bytes[] = {n_qk * esz, n_qk * esz, n_v * esz, n_qk * 4, n_b * 4,
+                                    h0 ? n_s * 4 : 0, n_v * esz, hT ? n_s * 4 : 0};
+        for (int i = 0; i < 8; i++)
+            if (overlaps(ckpt, n_c * 4, all[i], all_bytes[i]))
+                return fail(KDA_ERR_INVALID_ARG, "ckpt overlaps another tensor");
+    }
 
     kda::ChunkFwdArgs a{q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, d_status,
                         static_cast<cudaStream_t>(stream)};
+    a.ckpt = ckpt;
+    a.ckpt_every = ckpt ? ckpt_every : 0;
     cudaError_t e = io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
                                    : kda::launch_chunk_fwd_simt(a, io);
     if (e != cudaSuccess) {
@@ -124,6 +142,29 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const fl
         return KDA_ERR_CUDA;
     }
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* h0, void* o, float* hT, int B,
+                           int T, int H, int dk, int dv, kda_dtype_t io, void* workspace,
+                           size_t ws_bytes, int* d_status, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0,
+                          d_status, stream);
+}
+
+kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* h0, void* o, float* hT,
+                                float* ckpt, int ckpt_every, int B, int T, int H, int dk, int dv,
+                                kda_dtype_t io, int* d_status, void* stream) {
+    if (!ckpt) return fail(KDA_ERR_INVALID_ARG, "ckpt must be non-NULL");
+    return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, ckpt, ckpt_every,
+                          d_status, stream);
 }
 
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,

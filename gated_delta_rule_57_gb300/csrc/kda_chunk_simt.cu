@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(NT, 1)
                           const TIn* __restrict__ v, const float* __restrict__ g,
                           const float* __restrict__ beta, const float* __restrict__ h0,
                           TIn* __restrict__ o, float* __restrict__ hT, int T, int H, int DV,
-                          int* __restrict__ d_status) {
+                          int* __restrict__ d_status, float* __restrict__ ckpt, int ckpt_every) {
     using Sm = SimtSmem<DK, DVS, C>;
     constexpr int LDK = Sm::LDK, LDV = Sm::LDV, LDC = Sm::LDC, NTL = Sm::NTL;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -249,6 +249,15 @@ __global__ void __launch_bounds__(NT, 1)
             for (int s = 0; s < C; s++) acc += sm.Ke[s * LDK + i] * sm.V[s * LDV + j];
             sm.S[i * LDV + j] = acc;
         }
+        if (ckpt && (t0 + C) % ckpt_every == 0 && t0 + C <= T) {  // sparse state checkpoint
+            __syncthreads();
+            const int n_ckpt = T / ckpt_every, jc = (t0 + C) / ckpt_every - 1;
+            float* dst = ckpt + (((size_t)b * H + h) * n_ckpt + jc) * DK * DV;
+            for (int idx = tid; idx < DK * DVS; idx += NT) {
+                const int i = idx / DVS, j = idx % DVS;
+                dst[(size_t)i * DV + j0 + j] = sm.S[i * LDV + j];
+            }
+        }
     }
     __syncthreads();
     report_flags(d_status, flags);
@@ -272,7 +281,8 @@ cudaError_t launch_t(const ChunkFwdArgs& a) {
     dim3 grid(a.dv / DVS, a.H, a.B);
     kern<<<grid, NT, smem, a.stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
-        a.g, a.beta, a.h0, static_cast<TIn*>(a.o), a.hT, a.T, a.H, a.dv, a.d_status);
+        a.g, a.beta, a.h0, static_cast<TIn*>(a.o), a.hT, a.T, a.H, a.dv, a.d_status, a.ckpt,
+        a.ckpt_every);
     return cudaGetLastError();
 }
 

@@ -88,6 +88,9 @@ struct TcParams {
     float* hT;
     int T, H;
     int* d_status;
+    float* ckpt;    // [B, H, n_ckpt, dk, dv] or null
+    int ck_chunks;  // chunks between checkpoints
+    int n_ckpt;
 };
 
 // 2^x on the SFU (ex2.approx, flush-to-zero). Arguments here are log2-decays
@@ -720,6 +723,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
+        // Sparse state checkpoint: only full chunks count, so the slot index
+        // stays below n_ckpt = T / ckpt_every.
+        if (p.ckpt && (c + 1) % p.ck_chunks == 0 && (c + 1) / p.ck_chunks <= p.n_ckpt) {
+            const int jc = (c + 1) / p.ck_chunks - 1;
+            float* dst = p.ckpt + (((size_t)blockIdx.x * p.n_ckpt + jc) * kD + lane) * kD + 32 * u;
+#pragma unroll
+            for (int cc = 0; cc < 32; cc += 16) {
+                float x[16];
+                tmem_ld16(tq + TM_S + 32 * u + cc, x);
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 4)
+                    *reinterpret_cast<float4*>(dst + cc + jj) =
+                        make_float4(x[jj], x[jj + 1], x[jj + 2], x[jj + 3]);
+            }
+            tc_fence_before();
+        }
     }
 
     if (failed) flags |= KDA_DEV_TIMEOUT;
@@ -776,7 +795,8 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, 
 
 cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
     if (a.dk != kD || a.dv != kD) return launch_chunk_fwd_simt(a, KDA_BF16);
-    TcParams p{a.beta, a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.T, a.H, a.d_status};
+    TcParams p{a.beta, a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.T, a.H, a.d_status,
+               a.ckpt, a.ckpt ? a.ckpt_every / kC : 1, a.ckpt ? a.T / a.ckpt_every : 0};
     CUtensorMap mq{}, mk{}, mv{}, mg{};
     if (a.T > 0) {
         const int T = a.T;

@@ -24,6 +24,8 @@ struct ChunkFwdArgs {
     int B, T, H, dk, dv;
     int* d_status;  // may be null
     cudaStream_t stream;
+    float* ckpt = nullptr;  // [B, H, T / ckpt_every, dk, dv] or null
+    int ckpt_every = 0;     // tokens between checkpoints (multiple of 64)
 };
 
 struct DecodeArgs {

@@ -76,6 +76,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, vp,
                                         sz, vp, vp]
             L.kda_chunk_fwd.restype = I
+            L.kda_chunk_fwd_ckpt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I,
+                                             I, vp, vp]
+            L.kda_chunk_fwd_ckpt.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
             L.kda_decode_step.restype = I
             L.kda_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I,
@@ -145,6 +148,32 @@ def kda_chunk_fwd(q, k, v, g, beta, h0=None, *, o=None, hT=None, want_hT: bool =
                                ws_bytes, _ptr(status), _stream(stream))
     _check(code)
     return o, hT
+
+
+def kda_chunk_fwd_ckpt(q, k, v, g, beta, h0=None, *, ckpt_every: int, o=None, hT=None,
+                       ckpt=None, want_hT: bool = True, status: Optional[torch.Tensor] = None,
+                       stream=None):
+    """kda_chunk_fwd that also returns the state every `ckpt_every` tokens.
+
+    Returns (o, hT, ckpt) with ckpt [B, H, T // ckpt_every, dk, dv] fp32.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if ckpt is None:
+        n = T // ckpt_every if ckpt_every > 0 else 0
+        ckpt = torch.empty((B, H, max(n, 0), dk, dv), dtype=torch.float32, device=q.device)
+    code = lib().kda_chunk_fwd_ckpt(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(o), _ptr(hT), _ptr(ckpt), int(ckpt_every), B, T, H, dk,
+                                    dv, io, _ptr(status), _stream(stream))
+    _check(code)
+    return o, hT, ckpt
 
 
 def kda_decode_step(q, k, v, g, beta, S, *, o=None, status: Optional[torch.Tensor] = None,

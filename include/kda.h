@@ -121,6 +121,26 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const fl
                            size_t ws_bytes, int* d_status, void* stream);
 
 /*
+ * kda_chunk_fwd that also saves the state at sparse boundaries: the state
+ * after token (j + 1) * ckpt_every - 1 goes to ckpt[b, h, j] for
+ * j = 0 .. T / ckpt_every - 1 (section "The bill arrives in the serving
+ * stack", second bullet: prefix reuse hashes every 512 tokens but keeps a
+ * recurrent-state restore point only at a sparse subset of those boundaries).
+ *
+ *   ckpt       : [B, H, T / ckpt_every, dk, dv] fp32 (out; must not overlap
+ *                any other tensor); the last entry equals hT when ckpt_every
+ *                divides T
+ *   ckpt_every : positive multiple of 64 (the chunk length), e.g. 512 or 2048
+ *
+ * Other arguments as for kda_chunk_fwd (no workspace is needed). Each
+ * checkpoint adds dk * dv * 4 bytes of writes per (b, h).
+ */
+kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* h0, void* o, float* hT,
+                                float* ckpt, int ckpt_every, int B, int T, int H, int dk, int dv,
+                                kda_dtype_t io, int* d_status, void* stream);
+
+/*
  * One decode step for N sequences (one token each), state updated in place
  * (section "The bill arrives in the serving stack", third bullet: the state
  * is overwritten where it lives).

@@ -21,7 +21,8 @@ def L():
 
 def test_exports_every_header_symbol(L):
     names = kda.header_functions()
-    assert {"kda_chunk_fwd", "kda_decode_step", "kda_decode_multi", "kda_chunk_fwd_workspace_size",
+    assert {"kda_chunk_fwd", "kda_chunk_fwd_ckpt", "kda_decode_step", "kda_decode_multi",
+            "kda_chunk_fwd_workspace_size",
             "kda_status_string", "kda_abi_version", "kda_last_error_string"} <= set(names)
     for n in names:
         assert hasattr(L, n), f"libkda.so does not export {n}"
@@ -128,3 +129,23 @@ def test_decode_multi_rejects(L, kw, code):
 
 def test_decode_multi_empty_is_a_no_op(L):
     assert call_multi(L, K=0, q=None) == ST.KDA_OK
+
+
+def call_ckpt(L, ckpt=A[7], every=128, T=256, **kw):
+    a = dict(q=A[0], k=A[1], v=A[2], g=A[3], beta=A[4], h0=None, o=A[5], hT=A[6], B=1, H=1,
+             dk=128, dv=128, io=kda.KDA_BF16)
+    a.update(kw)
+    return L.kda_chunk_fwd_ckpt(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["o"],
+                                a["hT"], ckpt, every, a["B"], T, a["H"], a["dk"], a["dv"],
+                                a["io"], None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ckpt=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(every=100), ST.KDA_ERR_INVALID_ARG),     # not a multiple of the chunk
+    (dict(every=0), ST.KDA_ERR_INVALID_ARG),
+    (dict(ckpt=A[7] + 4), ST.KDA_ERR_INVALID_ARG),  # misaligned
+    (dict(ckpt=A[2]), ST.KDA_ERR_INVALID_ARG),      # overlaps v
+])
+def test_chunk_fwd_ckpt_rejects(L, kw, code):
+    assert call_ckpt(L, **kw) == code

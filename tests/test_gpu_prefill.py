@@ -188,3 +188,34 @@ def test_status_flags(io, bad, flag):
     kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("io,d,every", [("bf16", 128, 64), ("bf16", 128, 128), ("f32", 64, 64),
+                                        ("f32", 128, 128), ("bf16", 64, 64)])
+def test_state_checkpoints(io, d, every):
+    """ckpt[b, h, j] is the state after token (j + 1) * every - 1 (oracle prefix)."""
+    w = small(io, d, True)
+    T = 330
+    x = inputs.prefill_inputs(w, "cpu", B=2, T=T, H=2, seed=31)
+    xd = {n: t.to(DEV) for n, t in x.items()}
+    o, hT, ck = kda.kda_chunk_fwd_ckpt(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"],
+                                       ckpt_every=every)
+    o2, h2 = kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"])
+    torch.cuda.synchronize()
+    assert ck.shape == (2, 2, T // every, d, d)
+    assert torch.equal(o, o2) and torch.equal(hT, h2)  # checkpoints change nothing else
+    dt = inputs.io_dtype(io)
+    for j in range(T // every):
+        n = (j + 1) * every
+        _, h_ref = oracle.prefill(x["q"][:, :n], x["k"][:, :n], x["v"][:, :n], x["g"][:, :n],
+                                  x["beta"][:, :n], x["h0"])
+        assert_s(ck[:, :, j], h_ref, dt, f"checkpoint {j}")
+
+
+def test_checkpoint_at_end_equals_hT():
+    w = small("bf16", 128, True)
+    x = inputs.prefill_inputs(w, DEV, B=1, T=256, H=3, seed=32)
+    o, hT, ck = kda.kda_chunk_fwd_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                       ckpt_every=128)
+    torch.cuda.synchronize()
+    assert torch.equal(ck[:, :, -1], hT)
