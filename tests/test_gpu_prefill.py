@@ -219,3 +219,72 @@ def test_checkpoint_at_end_equals_hT():
                                        ckpt_every=128)
     torch.cuda.synchronize()
     assert torch.equal(ck[:, :, -1], hT)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_degenerate_inputs(io):
+    """k = 0: the state only decays; v = 0 with h0 = 0: all zero; q = 0: o = 0."""
+    w = small(io, 128, True)
+    x = inputs.prefill_inputs(w, "cpu", B=1, T=150, H=2, seed=33)
+    dt = inputs.io_dtype(io)
+    xk = dict(x)
+    xk["k"] = torch.zeros_like(x["k"])
+    xd = {n: t.to(DEV) for n, t in xk.items()}
+    o, hT = kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"])
+    torch.cuda.synchronize()
+    ref = torch.exp(x["g"].double().sum(1))[..., None] * x["h0"].double()
+    assert_s(hT, ref.numpy(), dt, "k = 0 state")
+    o_ref, _ = oracle.prefill(xk["q"], xk["k"], xk["v"], xk["g"], xk["beta"], xk["h0"])
+    assert_o(o, o_ref, dt, "k = 0 output")
+    xv = {n: t.to(DEV) for n, t in x.items()}
+    xv["v"].zero_()
+    o, hT = kda.kda_chunk_fwd(xv["q"], xv["k"], xv["v"], xv["g"], xv["beta"], None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(o) == 0 and torch.count_nonzero(hT) == 0
+    xq = {n: t.to(DEV) for n, t in x.items()}
+    xq["q"].zero_()
+    o, _ = kda.kda_chunk_fwd(xq["q"], xq["k"], xq["v"], xq["g"], xq["beta"], xq["h0"])
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(o) == 0
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_exact_overwrite_orthonormal_keys(io):
+    """g = 0, beta = 1 and exactly orthonormal keys (entries +-0.5, exact in
+    bf16): writing (k, v) then reading with q = k returns v; rewriting a key
+    replaces its value. Holds across chunk boundaries (T = 200)."""
+    d, T = 128, 200
+    H4 = torch.tensor([[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]],
+                      dtype=torch.float32) / 2
+    K = torch.block_diag(*([H4] * (d // 4)))  # d exactly orthonormal rows
+    gen = torch.Generator().manual_seed(34)
+    idx = torch.randint(0, d, (T,), generator=gen)
+    dt = inputs.io_dtype(io)
+    k = K[idx][None, :, None, :].to(dt)
+    q = k.clone()
+    v = torch.randint(-4, 5, (1, T, 1, d), generator=gen).float().to(dt)
+    g = torch.zeros(1, T, 1, d)
+    beta = torch.ones(1, T, 1)
+    o, hT = kda.kda_chunk_fwd(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), None)
+    torch.cuda.synchronize()
+    assert_o(o, v.double().numpy(), dt, "read-back of the value just written")
+    latest = {}
+    for t in range(T):
+        latest[int(idx[t])] = v[0, t, 0].double()
+    S = sum(torch.outer(K[i].double(), val) for i, val in latest.items())
+    assert_s(hT, S.numpy()[None, None], dt, "overwritten state")
+
+
+def test_many_heads():
+    """B*H = 2048 sequences (8 waves of CTAs) against the oracle on sampled heads."""
+    w = inputs.PrefillWorkload("many", 16, 130, 128, 128, 128, "bf16", 35, h0_std=0.02)
+    x = inputs.prefill_inputs(w, DEV)
+    o, hT = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    torch.cuda.synchronize()
+    heads = [0, 77, 127]
+    bsel = [0, 9, 15]
+    sub = {n: x[n][bsel][:, :, heads].contiguous().cpu() for n in ("q", "k", "v", "g", "beta")}
+    h0s = x["h0"][bsel][:, heads].contiguous().cpu()
+    o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], h0s)
+    assert_o(o[bsel][:, :, heads], o_ref, torch.bfloat16)
+    assert_s(hT[bsel][:, heads], h_ref, torch.bfloat16)
