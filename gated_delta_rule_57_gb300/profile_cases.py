@@ -2,10 +2,13 @@
 
     python -m gated_delta_rule_57_gb300.profile_cases prefill [--B 8] [--calls 4]
     python -m gated_delta_rule_57_gb300.profile_cases decode  [--calls 4]
+    python -m gated_delta_rule_57_gb300.profile_cases spec    [--calls 4]
 
 Draws the seeded synthetic inputs on the GPU, then makes `calls` back-to-back
 calls of kda_chunk_fwd (prefill: B x 8192 tokens x 32 heads, d = 128, bf16)
-or kda_decode_step (256 sequences x 32 heads, d = 128). Under a profiler,
+or kda_decode_step (256 sequences x 32 heads, d = 128), or rounds of
+kda_decode_multi (the same 256 x 32 states, 4 draft tokens: verify then
+commit). Under a profiler,
 skip the first calls as warm-up (e.g. ncu -s 2 -c 1 -k regex:kda_).
 """
 import argparse
@@ -17,7 +20,7 @@ from . import inputs, kda
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("which", choices=["prefill", "decode"])
+    ap.add_argument("which", choices=["prefill", "decode", "spec"])
     ap.add_argument("--B", type=int, default=8)
     ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
@@ -29,11 +32,19 @@ def main():
         hT = torch.empty(args.B, w.H, w.dk, w.dv, device=dev)
         for _ in range(args.calls):
             kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o=o, hT=hT)
-    else:
+    elif args.which == "decode":
         w = inputs.DECODE_N256
         x = inputs.decode_inputs(w, dev, steps=args.calls)
         for s in range(args.calls):
             kda.kda_decode_step(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], x["S"])
+    else:
+        w = inputs.DECODE_N256
+        x = inputs.prefill_inputs(inputs.PrefillWorkload("draft", w.N, 4, w.H, w.dk, w.dv, w.io,
+                                                         w.seed, h0_std=w.S_std), dev)
+        for _ in range(args.calls):
+            kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+            kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], commit=True,
+                                 want_o=False)
     torch.cuda.synchronize()
     print(f"{args.which}: {args.calls} calls done")
 
