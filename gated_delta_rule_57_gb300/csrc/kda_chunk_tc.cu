@@ -17,15 +17,18 @@
 //   A_rs = b_r sum_c k_rc k_sc e^{G_rc-G_sc} (s<r),  P_rs = sum_c q_rc k_sc e^{G_rc-G_sc} (s<=r)
 //   T' = (I + A)^-1 Diag(b),  Kt = k e^{G},  Qt = q e^{G},  Kb = k e^{G_C - G}
 //   W = T' Kt,  Ut = T' V,  U = Ut - W S0,  O = Qt S0 + P U,  S_C = Diag(e^{G_C}) S0 + Kb^T U.
-// Rewritten for 128-row MMAs with X = P T':
+// Rewritten for 128-row MMAs (0 = a 64-row block of zeros):
 //   round 1  Gram blocks  [Kp; Qp] * [Km_0; Km_1; Km_2; Km_3]^T   (N = 16+32+48+64)
-//   round 2  X      = [T'; P] * T'          (rows 64..127 used)
-//   round 3  [Ut; P Ut | W; PW] = [T'; X] * [V | Kt]   (N = 256: D1, then scratch)
-//   round 4  D1    += [-W; Qt - PW] * S0   ->  D1 = [U; O]
+//   round 3  [0; Ut | 0; W] = [0; T'] * [V | Kt]   (N = 256: D1, then scratch)
+//   round 4  D1    += [Qt; -W] * S0         ->  D1 = [Qt S0; U]
 //   round 5  S     += Kb^T * U              (S pre-scaled by e^{G_C} in TMEM)
+//            D1    += [P; 0] * U            ->  D1 = [O; U]
+// (Round numbers follow an earlier form with a round 2 for X = P T'; folding
+// P U into round 5 removed it from the per-chunk chain.) The O rows are read
+// out while the next chunk's round 1 runs.
 //
 // Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
-// lane quarter), ~207 KB of shared memory (one CTA per SM), 416 TMEM columns:
+// lane quarter), ~212 KB of shared memory (one CTA per SM), 416 TMEM columns:
 // the fp32 state S (128 lanes x 128 columns) stays in tensor memory for the
 // whole sequence. Inputs arrive by TMA with the 128-byte swizzle (q, k, v in
 // the layout the MMA descriptors expect; g in 32-channel blocks); the next
@@ -53,28 +56,31 @@ constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; the
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
 constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch | A1
 constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
-constexpr uint32_t OFF_KT = 122880;    // Kt, SW128 64 x 128            } S0 bf16 copy
-constexpr uint32_t OFF_A0 = 139264;    // [T'; P -> X], SW128 128 x 64  } after round 3
-constexpr uint32_t OFF_KB = 155648;    // Kb, SW128 64 x 128 (MN-major A)
-constexpr uint32_t OFF_QT = 172032;    // Qt, SW128 64 x 128
-constexpr uint32_t OFF_U = 188416;     // U, SW128 64 x 128 (MN-major B)
-constexpr uint32_t OFF_BETA = 204800;  // fp32 [64]
-constexpr uint32_t OFF_LAM = 205056;   // fp32 [128]  e^{G_C}
-constexpr uint32_t OFF_GT = 205568;    // fp32 [4][128] tile log2-decay totals
-constexpr uint32_t SMEM_BYTES = 207616 + 1024;
-// aliases inside OFF_KM (solve scratch lives between round 1 and round 2; A1
-// between round 3 and round 4)
+constexpr uint32_t OFF_KT = 122880;    // Kt, SW128 64 x 128
+constexpr uint32_t OFF_A0 = 139264;    // [P; 0; T'], SW128 192 x 64 (K-major A)
+constexpr uint32_t OFF_KB = 163840;    // Kb, SW128 64 x 128 (MN-major A)
+constexpr uint32_t OFF_A1 = 180224;    // [Qt; -W], SW128 128 x 128; then U (64 x 128, MN-major B)
+constexpr uint32_t OFF_BETA = 212992;  // fp32 [64]
+constexpr uint32_t OFF_LAM = 213248;   // fp32 [128]  e^{G_C}
+constexpr uint32_t OFF_GT = 213760;    // fp32 [4][128] tile log2-decay totals
+constexpr uint32_t SMEM_BYTES = 215808 + 1024;
+// Rows of the A0 tile: P at 0..63, zeros at 64..127 (written once), T' at
+// 128..191. [0; T'] and [P; 0] are both 128-row operands inside it.
+constexpr uint32_t A0_ZERO = 8192, A0_TP = 16384;
+constexpr uint32_t OFF_U = OFF_A1;  // A1 is dead once round 4 has completed
+// aliases inside OFF_KM (solve scratch lives between round 1 and the end of
+// the solve; the S0 copy between round 3 and round 4)
 constexpr int LDA = 65;  // fp32 A: odd stride, column walks are conflict-free
 constexpr int LDT = 68;  // fp32 T: 16-byte rows for float4 strips
 constexpr int LDM = 52;
 constexpr uint32_t OFF_FA = OFF_KM;           // fp32 A [64][65]
 constexpr uint32_t OFF_FT = OFF_KM + 16640;   // fp32 T [64][68]
 constexpr uint32_t OFF_MS = OFF_KM + 34048;   // fp32 [16][52] block-row product
-constexpr uint32_t OFF_A1 = OFF_KM;           // [-W; Q'], SW128 128 x 128
-constexpr uint32_t OFF_S = OFF_KT;            // S0 bf16, SW128 128 x 128 (MN-major B)
+constexpr uint32_t OFF_S = OFF_KM;            // S0 bf16, SW128 128 x 128 (MN-major B)
 constexpr int KM_ROWS = 160;                  // windows of 16, 32, 48, 64 rows
 __host__ __device__ __forceinline__ constexpr int win_row(int a) { return 8 * a * (a + 1); }
 static_assert(OFF_MS + 2 * 16 * LDM * 4 <= OFF_V, "solve scratch overflows the window buffer");
+static_assert(OFF_S + 32768 <= OFF_V, "S0 copy overflows the window buffer");
 
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
@@ -127,10 +133,6 @@ __device__ __forceinline__ void unpack8(uint4 u, float* x) {
 __device__ __forceinline__ void st_row8(unsigned char* tile, int r, int c0, int R,
                                         const float* x) {
     *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0, R)) = pack8(x);
-}
-__device__ __forceinline__ void ld_row8(const unsigned char* tile, int r, int c0, int R,
-                                        float* x) {
-    unpack8(*reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0, R)), x);
 }
 
 // Descriptors for the two operand orientations of an SW128 tile with R rows;
@@ -320,9 +322,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
     }
+    // The zero rows of A0 (8 KB: one 16-byte store per thread).
+    static_assert(kThreads * 16 == 8192, "zero block size");
+    *reinterpret_cast<uint4*>(sm + OFF_A0 + A0_ZERO + 16 * tid) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+
+    // O rows of chunk cc (D1 lanes 0..63, columns [32u, 32u + 32)) -> global.
+    auto store_o = [&](int cc, int len) {
+        float x[32];
+        tmem_ld32(tq + TM_D1 + 32 * u, x);
+        if (lane < len) {
+            __nv_bfloat16* dst = p.o + (((size_t)b * T + cc * kC + lane) * p.H + h) * kD + 32 * u;
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
+        }
+    };
 
     uint32_t mma_phase = 0;
     auto mma_wait = [&]() {
@@ -332,8 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int c = 0; c < nchunks && !failed; c++) {
-        const int t0 = c * kC;
-        const int L = min(kC, T - t0);
         const uint32_t par = (uint32_t)(c & 1);
 
         uint4 stash[2][3];
@@ -505,9 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 2; e++) {
             *reinterpret_cast<uint4*>(sm + OFF_KT + p1_off + p1_ro[e]) = stash[e][0];
-            *reinterpret_cast<uint4*>(sm + OFF_QT + p1_off + p1_ro[e]) = stash[e][1];
+            *reinterpret_cast<uint4*>(sm + OFF_A1 + 2 * p1_off + p1_ro[e]) = stash[e][1];
             *reinterpret_cast<uint4*>(sm + OFF_KB + p1_off + p1_ro[e]) = stash[e][2];
         }
+        // The previous (full) chunk's O rows, D1 lanes 0..63 -> global.
+        if (c > 0 && q < 2) store_o(c - 1, kC);
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -545,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float val = second ? v1[jj] : v0[jj];
                     out[jj] = (live && s <= r) ? val : 0.f;
                 }
-                st_row8(sm + OFF_A0, 64 + r, 16 * u, 128, out);
-                st_row8(sm + OFF_A0, 64 + r, 16 * u + 8, 128, out + 8);
+                st_row8(sm + OFF_A0, r, 16 * u, 128, out);
+                st_row8(sm + OFF_A0, r, 16 * u + 8, 128, out + 8);
             }
         }
         tc_fence_before();
@@ -557,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* FA = reinterpret_cast<const float*>(sm + OFF_FA);
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
+            unsigned char* TP = sm + OFF_A0 + A0_TP;
             if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
                 const int o0 = 16 * warp, jc = tid & 15;
                 float acc[16], x[16];
@@ -573,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
                         FT[(o0 + i) * LDT + o0 + jc] = x[i];
-                        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_A0 + sw128_offset(o0 + i, o0 + jc, 128)) =
+                        *reinterpret_cast<__nv_bfloat16*>(TP + sw128_offset(o0 + i, o0 + jc, 128)) =
                             __float2bfloat16_rn(x[i] * bj);
                     }
                 }
@@ -582,40 +600,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int blkid = e >> 7, i = (e >> 3) & 15, jp = e & 7;
                     const int br = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
                     const int bc = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-                    *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) = 0u;
+                    *reinterpret_cast<uint32_t*>(TP + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) = 0u;
                 }
             }
             __syncthreads();
-            merge_block_row<1>(FA, FT, MS, warp, tid & 31, sm + OFF_A0, sbeta);
-            merge_block_row<2>(FA, FT, MS, warp, tid & 31, sm + OFF_A0, sbeta);
-            merge_block_row<3>(FA, FT, MS, warp, tid & 31, sm + OFF_A0, sbeta);
+            merge_block_row<1>(FA, FT, MS, warp, tid & 31, TP, sbeta);
+            merge_block_row<2>(FA, FT, MS, warp, tid & 31, TP, sbeta);
+            merge_block_row<3>(FA, FT, MS, warp, tid & 31, TP, sbeta);
         }
         fence_proxy_async_smem();
-        __syncthreads();
-
-        // ------------------------------------------------------------ round 2: X = P T'
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
-            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);
-            const uint64_t bd0 = desc_mnmajor(sbase + OFF_A0, 128);
-#pragma unroll
-            for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
-                         kk > 0);
-            mma_commit(&bars[BAR_MMA]);
-        }
-        ok = mma_wait();
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (q >= 2) {  // rows 64..127 of X -> A0 rows 64..127, 16 columns per warp
-            float x[16];
-            tmem_ld16(tq + TM_SCR + 16 * u, x);
-            st_row8(sm + OFF_A0, lane, 16 * u, 128, x);
-            st_row8(sm + OFF_A0, lane, 16 * u + 8, 128, x + 8);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
         __syncthreads();
 
         // ------------------------------------------------------------ round 3
@@ -624,11 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             // v and Kt are adjacent 64-row tiles, i.e. one MN-major operand of
-            // N = 256 whose first half lands in D1 ([Ut; P Ut]) and second half
-            // in the scratch columns ([W; PW]).
+            // N = 256 whose first half lands in D1 ([0; Ut]) and second half
+            // in the scratch columns ([0; W]).
             static_assert(OFF_KT == OFF_V + 16384 && TM_SCR == TM_D1 + 128, "round-3 fusion layout");
             const uint32_t idesc = idesc_bf16(128, 256, 0, 1);
-            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);
+            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0 + A0_ZERO);
             const uint64_t bd0 = desc_mnmajor(sbase + OFF_V, 64);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
@@ -642,23 +635,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
 
         {
-            // [W; PW] columns [32u, 32u + 32) -> A1 = [-W; Qt - PW]
-            float x[32];
-            tmem_ld32(tq + TM_SCR + 32 * u, x);
-            if (lane < 64) {
+            if (q >= 2) {  // W (scratch lanes 64..127), columns [32u, 32u + 32) -> A1 rows 64..127
+                float x[32];
+                tmem_ld32(tq + TM_SCR + 32 * u, x);
 #pragma unroll
                 for (int e = 0; e < 32; e++) x[e] = -x[e];
-            } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    float qt[8];
-                    ld_row8(sm + OFF_QT, lane - 64, 32 * u + e, 64, qt);
-#pragma unroll
-                    for (int z = 0; z < 8; z++) x[e + z] = qt[z] - x[e + z];
-                }
+                for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, 32 * u + e, 128, x + e);
             }
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, 32 * u + e, 128, x + e);
             // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM
             float y[32];
             tmem_ld32(tq + TM_S + 32 * u, y);
@@ -675,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // ------------------------------------------------------------ round 4: [U; O]
+        // ------------------------------------------------------------ round 4: [Qt S0; U]
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
@@ -690,26 +674,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        {
+        if (q >= 2) {  // U rows (D1 lanes 64..127) -> bf16 operand
             float x[32];
             tmem_ld32(tq + TM_D1 + 32 * u, x);
-            if (lane < 64) {  // U rows -> bf16 operand
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_U, lane, 32 * u + e, 64, x + e);
-            } else {  // O rows -> global
-                const int r = lane - 64;
-                if (r < L) {
-                    __nv_bfloat16* dst = p.o + (((size_t)b * T + t0 + r) * p.H + h) * kD + 32 * u;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
-                }
-            }
+            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_U, lane - 64, 32 * u + e, 64, x + e);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ------------------------------------------------------------ round 5: S += Kb^T U
+        // ------------------------------------------------------------ round 5: S += Kb^T U, O += P U
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 128, 1, 1);
@@ -718,6 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16(tbase + TM_S, ad0 + kstep_mnmajor(kk), bd0 + kstep_mnmajor(kk), idesc, 1);
+            const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);
+            const uint64_t pd0 = desc_kmajor(sbase + OFF_A0);  // [P; 0]
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++)
+                mma_bf16(tbase + TM_D1, pd0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc_o,
+                         1);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
@@ -742,6 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (failed) flags |= KDA_DEV_TIMEOUT;
+    // O rows of the last chunk.
+    if (nchunks > 0 && !failed && q < 2) store_o(nchunks - 1, T - (nchunks - 1) * kC);
     // Final state -> hT.
     if (p.hT && !failed) {
         float* dst = p.hT + ((size_t)blockIdx.x * kD + lane) * kD + 32 * u;
