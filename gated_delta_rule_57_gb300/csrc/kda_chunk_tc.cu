@@ -85,7 +85,7 @@ static_assert(OFF_S + 32768 <= OFF_V, "S0 copy overflows the window buffer");
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
 
-enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, NBAR = 4 };
+enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R5 = 4, NBAR = 5 };
 
 struct TcParams {
     const float* beta;
@@ -347,6 +347,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_phase ^= 1u;
         return ok;
     };
+    // Round 5 completes on its own barrier and is waited for only when its
+    // results (S, the O rows, the U and Kb operands' buffers) are next needed,
+    // so the following chunk's decay scan and operand build run under it.
+    uint32_t r5_phase = 0;
+    bool r5_pending = false;
+    auto r5_wait = [&]() {
+        bool ok = true;
+        if (r5_pending) {
+            ok = mbar_wait(&bars[BAR_R5], r5_phase);
+            r5_phase ^= 1u;
+            r5_pending = false;
+        }
+        tc_fence_after();
+        return ok;
+    };
 
     for (int c = 0; c < nchunks && !failed; c++) {
         const uint32_t par = (uint32_t)(c & 1);
@@ -517,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
+        ok = r5_wait();  // Kb, U (under Qt) and D1 are free again
+        if (!ok) flags |= KDA_DEV_TIMEOUT;
 #pragma unroll
         for (int e = 0; e < 2; e++) {
             *reinterpret_cast<uint4*>(sm + OFF_KT + p1_off + p1_ro[e]) = stash[e][0];
@@ -524,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(sm + OFF_KB + p1_off + p1_ro[e]) = stash[e][2];
         }
         // The previous (full) chunk's O rows, D1 lanes 0..63 -> global.
-        if (c > 0 && q < 2) store_o(c - 1, kC);
-        ok = mma_wait();
+        if (c > 0 && q < 2 && ok) store_o(c - 1, kC);
+        ok = mma_wait() && ok;
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0 && c + 1 < nchunks) issue_qk(c + 1);
@@ -629,21 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
-        ok = mma_wait();
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
-
         {
-            if (q >= 2) {  // W (scratch lanes 64..127), columns [32u, 32u + 32) -> A1 rows 64..127
-                float x[32];
-                tmem_ld32(tq + TM_SCR + 32 * u, x);
-#pragma unroll
-                for (int e = 0; e < 32; e++) x[e] = -x[e];
-#pragma unroll
-                for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, 32 * u + e, 128, x + e);
-            }
-            // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM
+            // While round 3 runs (it touches neither S nor the window buffer):
+            // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM.
             float y[32];
             tmem_ld32(tq + TM_S + 32 * u, y);
 #pragma unroll
@@ -654,6 +659,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tq + TM_S + 32 * u, y);
             tmem_st16(tq + TM_S + 32 * u + 16, y + 16);
             tmem_wait_st();
+        }
+        ok = mma_wait();
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
+        if (q >= 2) {  // W (scratch lanes 64..127), columns [32u, 32u + 32) -> A1 rows 64..127
+            float x[32];
+            tmem_ld32(tq + TM_SCR + 32 * u, x);
+#pragma unroll
+            for (int e = 0; e < 32; e++) x[e] = -x[e];
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, 32 * u + e, 128, x + e);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -699,14 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16(tbase + TM_D1, pd0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc_o,
                          1);
-            mma_commit(&bars[BAR_MMA]);
+            mma_commit(&bars[BAR_R5]);
         }
-        ok = mma_wait();
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        r5_pending = true;
         // Sparse state checkpoint: only full chunks count, so the slot index
         // stays below n_ckpt = T / ckpt_every.
         if (p.ckpt && (c + 1) % p.ck_chunks == 0 && (c + 1) / p.ck_chunks <= p.n_ckpt) {
+            if (__syncthreads_or(!r5_wait())) { failed = true; break; }
             const int jc = (c + 1) / p.ck_chunks - 1;
             float* dst = p.ckpt + (((size_t)blockIdx.x * p.n_ckpt + jc) * kD + lane) * kD + 32 * u;
 #pragma unroll
@@ -722,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (!failed && r5_pending && __syncthreads_or(!r5_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
     if (nchunks > 0 && !failed && q < 2) store_o(nchunks - 1, T - (nchunks - 1) * kC);
