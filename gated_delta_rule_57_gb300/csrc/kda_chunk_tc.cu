@@ -166,66 +166,115 @@ __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// One block row of the blocked triangular inverse T = (I + A)^-1 (AB = 1..3):
-// with the diagonal blocks and block rows < AB known,
-//   M         = A[AB, <AB] T[<AB, <AB]    (16 x 16AB)
-//   T[AB,<AB] = -T[AB, AB] M
-// Warp w < 2AB owns the 8 output columns 8w..8w+7. Blocks of T above the
-// diagonal are never read (the K loop starts at the output's column block);
-// the finished block row also goes out as T' = T Diag(beta) in bf16.
-template <int AB>
-__device__ __forceinline__ void merge_block_row(const float* FA, float* FT, float* MS, int warp,
-                                                int lane, unsigned char* A0, const float* sbeta) {
-    constexpr int RB = 16 * AB;
+// Blocked triangular inverse T = (I + A)^-1 over 16-row blocks, merged as a
+// tree: with the diagonal blocks T_ii known,
+//   level 2:  T_10 = -T_11 A_10 T_00          T_32 = -T_33 A_32 T_22
+//   level 3:  T_[23][01] = -T_[23][23] A_[23][01] T_[01][01]   (32 x 32 blocks)
+// Each level is two dependent 16-row products on the TF32 tensor path; a warp
+// computes the slab of the inner product that its own output tile needs into
+// private shared memory, so only the levels are separated by CTA barriers.
+// Blocks of T above the diagonal are never read; every finished block also
+// goes out as T' = T Diag(beta) in bf16.
+__device__ __forceinline__ void store_tprime(unsigned char* TP, const float* sbeta, int r, int n,
+                                             const float* acc) {
+    const float b0 = sbeta[n], b1 = sbeta[n + 1];
+    *reinterpret_cast<uint32_t*>(TP + sw128_offset(r, n, 128)) =
+        pack_bf16(-acc[0] * b0, -acc[1] * b1);
+    *reinterpret_cast<uint32_t*>(TP + sw128_offset(r + 8, n, 128)) =
+        pack_bf16(-acc[2] * b0, -acc[3] * b1);
+}
+
+// Warps 0..3: output tile (block i = 1 or 3, columns 8nt..8nt+7 of block i-1).
+__device__ __forceinline__ void solve_level2(const float* FA, float* FT, float* MS, int warp,
+                                             int lane, unsigned char* TP, const float* sbeta) {
+    if (warp >= 4) return;
     const int g = lane >> 2, t = lane & 3;
-    if (warp < 2 * AB) {
-        const int n0 = 8 * warp;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const float* ar0 = FA + (RB + g) * LDA;
-        const float* ar1 = FA + (RB + g + 8) * LDA;
+    const int i = (warp >> 1) ? 3 : 1, nt = warp & 1;
+    const int r0 = 16 * i, c0 = r0 - 16, n0 = c0 + 8 * nt;
+    float* M = MS + warp * 128;  // private 16 x 8
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 2 * AB; ks++) {
-            if (ks >= 2 * (warp >> 1)) {  // T[k, n] = 0 for k above n's 16-column block
-                const int k0 = 8 * ks;
-                const uint32_t af[4] = {to_tf32(ar0[k0 + t]), to_tf32(ar1[k0 + t]),
-                                        to_tf32(ar0[k0 + t + 4]), to_tf32(ar1[k0 + t + 4])};
-                const uint32_t bf[2] = {to_tf32(FT[(k0 + t) * LDT + n0 + g]),
-                                        to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
-                mma_tf32(acc, af, bf);
-            }
-        }
-        MS[g * LDM + n0 + 2 * t] = acc[0];
-        MS[g * LDM + n0 + 2 * t + 1] = acc[1];
-        MS[(g + 8) * LDM + n0 + 2 * t] = acc[2];
-        MS[(g + 8) * LDM + n0 + 2 * t + 1] = acc[3];
+    for (int ks = 0; ks < 2; ks++) {  // M = A_{i,i-1} T_{i-1,i-1}[:, n0..]
+        const int k0 = c0 + 8 * ks;
+        const uint32_t af[4] = {to_tf32(FA[(r0 + g) * LDA + k0 + t]),
+                                to_tf32(FA[(r0 + g + 8) * LDA + k0 + t]),
+                                to_tf32(FA[(r0 + g) * LDA + k0 + t + 4]),
+                                to_tf32(FA[(r0 + g + 8) * LDA + k0 + t + 4])};
+        const uint32_t bf[2] = {to_tf32(FT[(k0 + t) * LDT + n0 + g]),
+                                to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
+        mma_tf32(acc, af, bf);
     }
-    __syncthreads();
-    if (warp < 2 * AB) {
-        const int n0 = 8 * warp;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const float* tr0 = FT + (RB + g) * LDT + RB;
-        const float* tr1 = FT + (RB + g + 8) * LDT + RB;
+    M[g * 8 + 2 * t] = acc[0];
+    M[g * 8 + 2 * t + 1] = acc[1];
+    M[(g + 8) * 8 + 2 * t] = acc[2];
+    M[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    __syncwarp();
+    float out[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 2; ks++) {
+    for (int ks = 0; ks < 2; ks++) {  // T_{i,i-1} = -T_ii M
+        const int k0 = 8 * ks;
+        const uint32_t af[4] = {to_tf32(FT[(r0 + g) * LDT + r0 + k0 + t]),
+                                to_tf32(FT[(r0 + g + 8) * LDT + r0 + k0 + t]),
+                                to_tf32(FT[(r0 + g) * LDT + r0 + k0 + t + 4]),
+                                to_tf32(FT[(r0 + g + 8) * LDT + r0 + k0 + t + 4])};
+        const uint32_t bf[2] = {to_tf32(M[(k0 + t) * 8 + g]), to_tf32(M[(k0 + t + 4) * 8 + g])};
+        mma_tf32(out, af, bf);
+    }
+    FT[(r0 + g) * LDT + n0 + 2 * t] = -out[0];
+    FT[(r0 + g) * LDT + n0 + 2 * t + 1] = -out[1];
+    FT[(r0 + g + 8) * LDT + n0 + 2 * t] = -out[2];
+    FT[(r0 + g + 8) * LDT + n0 + 2 * t + 1] = -out[3];
+    store_tprime(TP, sbeta, r0 + g, n0 + 2 * t, out);
+}
+
+// Warps 0..7: output tile (16-row block 2 + rt, columns 8nt..8nt+7 of 0..31).
+// Rows 0..31 of A are dead by now; they hold the private slabs.
+__device__ __forceinline__ void solve_level3(float* FA, const float* FT, int warp, int lane,
+                                             unsigned char* TP, const float* sbeta) {
+    if (warp >= 8) return;
+    const int g = lane >> 2, t = lane & 3;
+    const int rt = warp >> 2, nt = warp & 3;
+    const int n0 = 8 * nt, kb = 2 * (nt >> 1);  // T[k, n0..] = 0 for k < 8 kb
+    float* M = FA + warp * 256;                  // private 32 x 8
+    static_assert(8 * 256 <= 32 * LDA, "level-3 slabs overlap live rows of A");
+#pragma unroll
+    for (int mt = 0; mt < 2; mt++) {  // M = A_[23][01] T_[01][01][:, n0..]
+        if (mt > rt) break;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int ra = 32 + 16 * mt;
+#pragma unroll
+        for (int ks = 0; ks < 4; ks++) {
+            if (ks < kb) continue;
             const int k0 = 8 * ks;
-            const uint32_t af[4] = {to_tf32(tr0[k0 + t]), to_tf32(tr1[k0 + t]),
-                                    to_tf32(tr0[k0 + t + 4]), to_tf32(tr1[k0 + t + 4])};
-            const uint32_t bf[2] = {to_tf32(MS[(k0 + t) * LDM + n0 + g]),
-                                    to_tf32(MS[(k0 + t + 4) * LDM + n0 + g])};
+            const uint32_t af[4] = {to_tf32(FA[(ra + g) * LDA + k0 + t]),
+                                    to_tf32(FA[(ra + g + 8) * LDA + k0 + t]),
+                                    to_tf32(FA[(ra + g) * LDA + k0 + t + 4]),
+                                    to_tf32(FA[(ra + g + 8) * LDA + k0 + t + 4])};
+            const uint32_t bf[2] = {to_tf32(FT[(k0 + t) * LDT + n0 + g]),
+                                    to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
             mma_tf32(acc, af, bf);
         }
-        FT[(RB + g) * LDT + n0 + 2 * t] = -acc[0];
-        FT[(RB + g) * LDT + n0 + 2 * t + 1] = -acc[1];
-        FT[(RB + g + 8) * LDT + n0 + 2 * t] = -acc[2];
-        FT[(RB + g + 8) * LDT + n0 + 2 * t + 1] = -acc[3];
-        // T' = T Diag(beta), straight into the bf16 MMA operand
-        const float b0 = sbeta[n0 + 2 * t], b1 = sbeta[n0 + 2 * t + 1];
-        *reinterpret_cast<uint32_t*>(A0 + sw128_offset(RB + g, n0 + 2 * t, 128)) =
-            pack_bf16(-acc[0] * b0, -acc[1] * b1);
-        *reinterpret_cast<uint32_t*>(A0 + sw128_offset(RB + g + 8, n0 + 2 * t, 128)) =
-            pack_bf16(-acc[2] * b0, -acc[3] * b1);
+        float* Mm = M + 16 * mt * 8;
+        Mm[g * 8 + 2 * t] = acc[0];
+        Mm[g * 8 + 2 * t + 1] = acc[1];
+        Mm[(g + 8) * 8 + 2 * t] = acc[2];
+        Mm[(g + 8) * 8 + 2 * t + 1] = acc[3];
     }
-    __syncthreads();
+    __syncwarp();
+    float out[4] = {0.f, 0.f, 0.f, 0.f};
+    const int r0 = 32 + 16 * rt;
+#pragma unroll
+    for (int ks = 0; ks < 4; ks++) {  // T_[23][01] = -T_[23][23] M
+        if (ks >= 2 * (rt + 1)) break;
+        const int k0 = 8 * ks;
+        const uint32_t af[4] = {to_tf32(FT[(r0 + g) * LDT + 32 + k0 + t]),
+                                to_tf32(FT[(r0 + g + 8) * LDT + 32 + k0 + t]),
+                                to_tf32(FT[(r0 + g) * LDT + 32 + k0 + t + 4]),
+                                to_tf32(FT[(r0 + g + 8) * LDT + 32 + k0 + t + 4])};
+        const uint32_t bf[2] = {to_tf32(M[(k0 + t) * 8 + g]), to_tf32(M[(k0 + t + 4) * 8 + g])};
+        mma_tf32(out, af, bf);
+    }
+    store_tprime(TP, sbeta, r0 + g, n0 + 2 * t, out);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -588,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ------------------------------------------------------------ T = (I + A)^-1
         {
-            const float* FA = reinterpret_cast<const float*>(sm + OFF_FA);
+            float* FA = reinterpret_cast<float*>(sm + OFF_FA);
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
             unsigned char* TP = sm + OFF_A0 + A0_TP;
@@ -621,9 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncthreads();
-            merge_block_row<1>(FA, FT, MS, warp, tid & 31, TP, sbeta);
-            merge_block_row<2>(FA, FT, MS, warp, tid & 31, TP, sbeta);
-            merge_block_row<3>(FA, FT, MS, warp, tid & 31, TP, sbeta);
+            solve_level2(FA, FT, MS, warp, tid & 31, TP, sbeta);
+            __syncthreads();
+            solve_level3(FA, FT, warp, tid & 31, TP, sbeta);
         }
         fence_proxy_async_smem();
         __syncthreads();
