@@ -70,16 +70,15 @@ constexpr uint32_t A0_ZERO = 8192, A0_TP = 16384;
 constexpr uint32_t OFF_U = OFF_A1;  // A1 is dead once round 4 has completed
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
 // the solve; the S0 copy between round 3 and round 4)
-constexpr int LDA = 65;  // fp32 A: odd stride, column walks are conflict-free
-constexpr int LDT = 68;  // fp32 T: 16-byte rows for float4 strips
-constexpr int LDM = 52;
-constexpr uint32_t OFF_FA = OFF_KM;           // fp32 A [64][65]
-constexpr uint32_t OFF_FT = OFF_KM + 16640;   // fp32 T [64][68]
-constexpr uint32_t OFF_MS = OFF_KM + 34048;   // fp32 [16][52] block-row product
+constexpr int LDA = 68;  // fp32 A: TF32 fragment loads (bank 4g + t) and float4 row stores conflict-free
+constexpr int LDT = 68;  // fp32 T: TF32 A-fragment loads conflict-free (B-fragment loads 2-way)
+constexpr uint32_t OFF_FA = OFF_KM;                 // fp32 A [64][LDA]
+constexpr uint32_t OFF_FT = OFF_FA + 64 * LDA * 4;  // fp32 T [64][LDT]
+constexpr uint32_t OFF_MS = OFF_FT + 64 * LDT * 4;  // fp32 level-2 slabs, 4 warps x [16][8]
 constexpr uint32_t OFF_S = OFF_KM;            // S0 bf16, SW128 128 x 128 (MN-major B)
 constexpr int KM_ROWS = 160;                  // windows of 16, 32, 48, 64 rows
 __host__ __device__ __forceinline__ constexpr int win_row(int a) { return 8 * a * (a + 1); }
-static_assert(OFF_MS + 2 * 16 * LDM * 4 <= OFF_V, "solve scratch overflows the window buffer");
+static_assert(OFF_MS + 4 * 128 * 4 <= OFF_V, "solve scratch overflows the window buffer");
 static_assert(OFF_S + 32768 <= OFF_V, "S0 copy overflows the window buffer");
 
 // TMEM columns.
@@ -204,10 +203,8 @@ __device__ __forceinline__ void solve_level2(const float* FA, float* FT, float* 
                                 to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
         mma_tf32(acc, af, bf);
     }
-    M[g * 8 + 2 * t] = acc[0];
-    M[g * 8 + 2 * t + 1] = acc[1];
-    M[(g + 8) * 8 + 2 * t] = acc[2];
-    M[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    *reinterpret_cast<float2*>(M + g * 8 + 2 * t) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2*>(M + (g + 8) * 8 + 2 * t) = make_float2(acc[2], acc[3]);
     __syncwarp();
     float out[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -255,10 +252,8 @@ __device__ __forceinline__ void solve_level3(float* FA, const float* FT, int war
             mma_tf32(acc, af, bf);
         }
         float* Mm = M + 16 * mt * 8;
-        Mm[g * 8 + 2 * t] = acc[0];
-        Mm[g * 8 + 2 * t + 1] = acc[1];
-        Mm[(g + 8) * 8 + 2 * t] = acc[2];
-        Mm[(g + 8) * 8 + 2 * t + 1] = acc[3];
+        *reinterpret_cast<float2*>(Mm + g * 8 + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2*>(Mm + (g + 8) * 8 + 2 * t) = make_float2(acc[2], acc[3]);
     }
     __syncwarp();
     float out[4] = {0.f, 0.f, 0.f, 0.f};
@@ -618,9 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float val = second ? v1[jj] : v0[jj];
                     out[jj] = (live && s < r) ? br * val : 0.f;
                 }
-                float* FA = reinterpret_cast<float*>(sm + OFF_FA) + r * LDA + 16 * u;
+                float4* FA = reinterpret_cast<float4*>(sm + OFF_FA + (r * LDA + 16 * u) * 4);
 #pragma unroll
-                for (int jj = 0; jj < 16; jj++) FA[jj] = out[jj];
+                for (int jj = 0; jj < 4; jj++)
+                    FA[jj] = make_float4(out[4 * jj], out[4 * jj + 1], out[4 * jj + 2], out[4 * jj + 3]);
             } else {
 #pragma unroll
                 for (int jj = 0; jj < 16; jj++) {
