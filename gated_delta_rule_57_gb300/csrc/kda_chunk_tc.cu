@@ -17,18 +17,19 @@
 //   A_rs = b_r sum_c k_rc k_sc e^{G_rc-G_sc} (s<r),  P_rs = sum_c q_rc k_sc e^{G_rc-G_sc} (s<=r)
 //   T' = (I + A)^-1 Diag(b),  Kt = k e^{G},  Qt = q e^{G},  Kb = k e^{G_C - G}
 //   W = T' Kt,  Ut = T' V,  U = Ut - W S0,  O = Qt S0 + P U,  S_C = Diag(e^{G_C}) S0 + Kb^T U.
-// Rewritten for 128-row MMAs (0 = a 64-row block of zeros):
+// Since W S0 = T' (Kt S0), the state enters only through Y = Kt S0 and
+// Qt S0, which need neither the Gram matrices nor the solve. As 128-row MMAs:
 //   round 1  Gram blocks  [Kp; Qp] * [Km_0; Km_1; Km_2; Km_3]^T   (N = 16+32+48+64)
-//   round 3  [0; Ut | 0; W] = [0; T'] * [V | Kt]   (N = 256: D1, then scratch)
-//   round 4  D1    += [Qt; -W] * S0         ->  D1 = [Qt S0; U]
-//   round 5  S     += Kb^T * U              (S pre-scaled by e^{G_C} in TMEM)
-//            D1    += [P; 0] * U            ->  D1 = [O; U]
-// (Round numbers follow an earlier form with a round 2 for X = P T'; folding
-// P U into round 5 removed it from the per-chunk chain.) The O rows are read
-// out while the next chunk's round 1 runs.
+//   round A  D1  = [Kt; Qt] * S0                  -> [Y; Qt S0]   (runs under the solve)
+//            V'  = V - Y  (bf16, in place of v; under the solve as well)
+//   round 3  SCR = [T'; P] * V'                   -> [U; -]      (U = Ut - W S0)
+//   round 5  S  += Kb^T * U                       (S pre-scaled by e^{G_C} in TMEM)
+//            D1 += [T'; P] * U                    -> [-; O]      (O = Qt S0 + P U)
+// The O rows are read out while the next chunk's round 1 runs. (Rounds 2
+// and 4 of earlier forms, X = P T' and [Qt; -W] S0, are gone.)
 //
 // Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
-// lane quarter), ~212 KB of shared memory (one CTA per SM), 416 TMEM columns:
+// lane quarter), ~220 KB of shared memory (one CTA per SM), 416 TMEM columns:
 // the fp32 state S (128 lanes x 128 columns) stays in tensor memory for the
 // whole sequence. Inputs arrive by TMA with the 128-byte swizzle (q, k, v in
 // the layout the MMA descriptors expect; g in 32-channel blocks); the next
@@ -49,6 +50,9 @@ using namespace ptx;
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
 constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
+// Round A is issued by warp 15, which has no other work during the solve
+// (issuing keeps a thread busy for about the MMA's duration).
+constexpr int kRoundAThread = kThreads - 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (bytes from a 1024-aligned base).
@@ -56,35 +60,31 @@ constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; the
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
 constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch | A1
 constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
-constexpr uint32_t OFF_KT = 122880;    // Kt, SW128 64 x 128
-constexpr uint32_t OFF_A0 = 139264;    // [P; 0; T'], SW128 192 x 64 (K-major A)
-constexpr uint32_t OFF_KB = 163840;    // Kb, SW128 64 x 128 (MN-major A)
-constexpr uint32_t OFF_A1 = 180224;    // [Qt; -W], SW128 128 x 128; then U (64 x 128, MN-major B)
-constexpr uint32_t OFF_BETA = 212992;  // fp32 [64]
-constexpr uint32_t OFF_LAM = 213248;   // fp32 [128]  e^{G_C}
-constexpr uint32_t OFF_GT = 213760;    // fp32 [4][128] tile log2-decay totals
-constexpr uint32_t SMEM_BYTES = 215808 + 1024;
-// Rows of the A0 tile: P at 0..63, zeros at 64..127 (written once), T' at
-// 128..191. [0; T'] and [P; 0] are both 128-row operands inside it.
-constexpr uint32_t A0_ZERO = 8192, A0_TP = 16384;
-constexpr uint32_t OFF_U = OFF_A1;  // A1 is dead once round 4 has completed
+constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major A)
+constexpr uint32_t OFF_KB = 139264;    // Kb, SW128 64 x 128 (MN-major A)
+constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major A); then U
+constexpr uint32_t OFF_S = 188416;     // S0 bf16, SW128 128 x 128 (MN-major B)
+constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
+constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
+constexpr uint32_t OFF_GT = 221952;    // fp32 [4][128] tile log2-decay totals
+constexpr uint32_t SMEM_BYTES = 224000 + 1024;
+// U (64 x 128, MN-major B) reuses [Kt; Qt] once round A has completed.
+constexpr uint32_t OFF_U = OFF_AKQ;
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
-// the solve; the S0 copy between round 3 and round 4)
+// the solve)
 constexpr int LDA = 68;  // fp32 A: TF32 fragment loads (bank 4g + t) and float4 row stores conflict-free
 constexpr int LDT = 68;  // fp32 T: TF32 A-fragment loads conflict-free (B-fragment loads 2-way)
 constexpr uint32_t OFF_FA = OFF_KM;                 // fp32 A [64][LDA]
 constexpr uint32_t OFF_FT = OFF_FA + 64 * LDA * 4;  // fp32 T [64][LDT]
 constexpr uint32_t OFF_MS = OFF_FT + 64 * LDT * 4;  // fp32 level-2 slabs, 4 warps x [16][8]
-constexpr uint32_t OFF_S = OFF_KM;            // S0 bf16, SW128 128 x 128 (MN-major B)
 constexpr int KM_ROWS = 160;                  // windows of 16, 32, 48, 64 rows
 __host__ __device__ __forceinline__ constexpr int win_row(int a) { return 8 * a * (a + 1); }
 static_assert(OFF_MS + 4 * 128 * 4 <= OFF_V, "solve scratch overflows the window buffer");
-static_assert(OFF_S + 32768 <= OFF_V, "S0 copy overflows the window buffer");
 
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
 
-enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R5 = 4, NBAR = 5 };
+enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R5 = 4, BAR_RA = 5, NBAR = 6 };
 
 struct TcParams {
     const float* beta;
@@ -132,6 +132,11 @@ __device__ __forceinline__ void unpack8(uint4 u, float* x) {
 __device__ __forceinline__ void st_row8(unsigned char* tile, int r, int c0, int R,
                                         const float* x) {
     *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0, R)) = pack8(x);
+}
+
+__device__ __forceinline__ void ld_row8(const unsigned char* tile, int r, int c0, int R,
+                                        float* x) {
+    unpack8(*reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0, R)), x);
 }
 
 // Descriptors for the two operand orientations of an SW128 tile with R rows;
@@ -366,20 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
     }
-    // The zero rows of A0 (8 KB: one 16-byte store per thread).
-    static_assert(kThreads * 16 == 8192, "zero block size");
-    *reinterpret_cast<uint4*>(sm + OFF_A0 + A0_ZERO + 16 * tid) = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // O rows of chunk cc (D1 lanes 0..63, columns [32u, 32u + 32)) -> global.
+    // O rows of chunk cc (D1 lanes 64..127, columns [32u, 32u + 32)) -> global.
     auto store_o = [&](int cc, int len) {
         float x[32];
         tmem_ld32(tq + TM_D1 + 32 * u, x);
-        if (lane < len) {
-            __nv_bfloat16* dst = p.o + (((size_t)b * T + cc * kC + lane) * p.H + h) * kD + 32 * u;
+        if (lane - 64 < len) {
+            __nv_bfloat16* dst =
+                p.o + (((size_t)b * T + cc * kC + lane - 64) * p.H + h) * kD + 32 * u;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
         }
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Round 5 completes on its own barrier and is waited for only when its
     // results (S, the O rows, the U and Kb operands' buffers) are next needed,
     // so the following chunk's decay scan and operand build run under it.
-    uint32_t r5_phase = 0;
+    uint32_t r5_phase = 0, ra_phase = 0;
     bool r5_pending = false;
     auto r5_wait = [&]() {
         bool ok = true;
@@ -576,16 +578,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                          idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
-        ok = r5_wait();  // Kb, U (under Qt) and D1 are free again
+        ok = r5_wait();  // Kb, U (under [Kt; Qt]), D1 and S are free again
         if (!ok) flags |= KDA_DEV_TIMEOUT;
 #pragma unroll
         for (int e = 0; e < 2; e++) {
-            *reinterpret_cast<uint4*>(sm + OFF_KT + p1_off + p1_ro[e]) = stash[e][0];
-            *reinterpret_cast<uint4*>(sm + OFF_A1 + 2 * p1_off + p1_ro[e]) = stash[e][1];
+            *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * p1_off + p1_ro[e]) = stash[e][0];
+            *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * p1_off + 8192 + p1_ro[e]) = stash[e][1];
             *reinterpret_cast<uint4*>(sm + OFF_KB + p1_off + p1_ro[e]) = stash[e][2];
         }
-        // The previous (full) chunk's O rows, D1 lanes 0..63 -> global.
-        if (c > 0 && q < 2 && ok) store_o(c - 1, kC);
+        // The previous (full) chunk's O rows, D1 lanes 64..127 -> global.
+        if (c > 0 && q >= 2 && ok) store_o(c - 1, kC);
+        if (ok) {
+            // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM.
+            float y[32];
+            tmem_ld32(tq + TM_S + 32 * u, y);
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_S, lane, 32 * u + e, 128, y + e);
+            const float lam = slam[lane];
+#pragma unroll
+            for (int e = 0; e < 32; e++) y[e] *= lam;
+            tmem_st16(tq + TM_S + 32 * u, y);
+            tmem_st16(tq + TM_S + 32 * u + 16, y + 16);
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
         ok = mma_wait() && ok;
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -624,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float val = second ? v1[jj] : v0[jj];
                     out[jj] = (live && s <= r) ? val : 0.f;
                 }
-                st_row8(sm + OFF_A0, r, 16 * u, 128, out);
-                st_row8(sm + OFF_A0, r, 16 * u + 8, 128, out + 8);
+                st_row8(sm + OFF_A0, 64 + r, 16 * u, 128, out);
+                st_row8(sm + OFF_A0, 64 + r, 16 * u + 8, 128, out + 8);
             }
         }
         tc_fence_before();
@@ -636,7 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* FA = reinterpret_cast<float*>(sm + OFF_FA);
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
-            unsigned char* TP = sm + OFF_A0 + A0_TP;
+            unsigned char* TP = sm + OFF_A0;  // T' rows 0..63
+            if (tid == kRoundAThread) {
+                // Round A: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+                const uint64_t ad0 = desc_kmajor(sbase + OFF_AKQ);
+                const uint64_t bd0 = desc_mnmajor(sbase + OFF_S, 128);
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++)
+                    mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk),
+                             idesc, kk > 0);
+                mma_commit(&bars[BAR_RA]);
+            }
             if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
                 const int o0 = 16 * warp, jc = tid & 15;
                 float acc[16], x[16];
@@ -657,8 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __float2bfloat16_rn(x[i] * bj);
                     }
                 }
-            } else {  // T' is zero in the six blocks above the diagonal
-                for (int e = tid - 128; e < 6 * 128; e += kThreads - 128) {
+            } else if (warp < 15) {  // T' is zero in the six blocks above the diagonal
+                for (int e = tid - 128; e < 6 * 128; e += kThreads - 160) {
                     const int blkid = e >> 7, i = (e >> 3) & 15, jp = e & 7;
                     const int br = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
                     const int bc = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
@@ -669,78 +697,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             solve_level2(FA, FT, MS, warp, tid & 31, TP, sbeta);
             __syncthreads();
             solve_level3(FA, FT, warp, tid & 31, TP, sbeta);
+            if (warp >= 8 && q < 2) {
+                // V' = V - Y for token rows lane (0..63), value columns [64 hv, 64 hv + 64),
+                // in place of v, by the four warps that are idle in this level.
+                ok = mbar_wait(&bars[BAR_V], par);
+                ok = mbar_wait(&bars[BAR_RA], ra_phase) && ok;
+                tc_fence_after();
+                const int hv = (warp >> 2) & 1;
+                if (ok) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; h2++) {
+                        const int c0 = 64 * hv + 32 * h2;
+                        float y[32];
+                        tmem_ld32(tq + TM_D1 + c0, y);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            float vv[8];
+                            ld_row8(sm + OFF_V, lane, c0 + e, 64, vv);
+#pragma unroll
+                            for (int z = 0; z < 8; z++) vv[z] -= y[e + z];
+                            st_row8(sm + OFF_V, lane, c0 + e, 64, vv);
+                        }
+                    }
+                }
+            }
+            ra_phase ^= 1u;
         }
         fence_proxy_async_smem();
-        __syncthreads();
-
-        // ------------------------------------------------------------ round 3
-        ok = mbar_wait(&bars[BAR_V], par);
+        tc_fence_before();
         if (__syncthreads_or(!ok)) { failed = true; break; }
+
+        // ------------------------------------------------------------ round 3: U = T' V'
         if (tid == 0) {
             tc_fence_after();
-            // v and Kt are adjacent 64-row tiles, i.e. one MN-major operand of
-            // N = 256 whose first half lands in D1 ([0; Ut]) and second half
-            // in the scratch columns ([0; W]).
-            static_assert(OFF_KT == OFF_V + 16384 && TM_SCR == TM_D1 + 128, "round-3 fusion layout");
-            const uint32_t idesc = idesc_bf16(128, 256, 0, 1);
-            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0 + A0_ZERO);
+            const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);  // [T'; P]
             const uint64_t bd0 = desc_mnmajor(sbase + OFF_V, 64);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
+                mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
                          kk > 0);
             mma_commit(&bars[BAR_MMA]);
-        }
-        {
-            // While round 3 runs (it touches neither S nor the window buffer):
-            // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM.
-            float y[32];
-            tmem_ld32(tq + TM_S + 32 * u, y);
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_S, lane, 32 * u + e, 128, y + e);
-            const float lam = slam[lane];
-#pragma unroll
-            for (int e = 0; e < 32; e++) y[e] *= lam;
-            tmem_st16(tq + TM_S + 32 * u, y);
-            tmem_st16(tq + TM_S + 32 * u + 16, y + 16);
-            tmem_wait_st();
         }
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
-        if (q >= 2) {  // W (scratch lanes 64..127), columns [32u, 32u + 32) -> A1 rows 64..127
+        if (q < 2) {  // U rows (scratch lanes 0..63) -> bf16 operand
             float x[32];
             tmem_ld32(tq + TM_SCR + 32 * u, x);
 #pragma unroll
-            for (int e = 0; e < 32; e++) x[e] = -x[e];
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_A1, lane, 32 * u + e, 128, x + e);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ------------------------------------------------------------ round 4: [Qt S0; U]
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
-            const uint64_t ad0 = desc_kmajor(sbase + OFF_A1);
-            const uint64_t bd0 = desc_mnmajor(sbase + OFF_S, 128);
-#pragma unroll
-            for (int kk = 0; kk < 8; kk++)
-                mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
-                         1);
-            mma_commit(&bars[BAR_MMA]);
-        }
-        ok = mma_wait();
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (q >= 2) {  // U rows (D1 lanes 64..127) -> bf16 operand
-            float x[32];
-            tmem_ld32(tq + TM_D1 + 32 * u, x);
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_U, lane - 64, 32 * u + e, 64, x + e);
+            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_U, lane, 32 * u + e, 64, x + e);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -756,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16(tbase + TM_S, ad0 + kstep_mnmajor(kk), bd0 + kstep_mnmajor(kk), idesc, 1);
             const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);
-            const uint64_t pd0 = desc_kmajor(sbase + OFF_A0);  // [P; 0]
+            const uint64_t pd0 = desc_kmajor(sbase + OFF_A0);  // [T'; P]: rows 0..63 of D1 are dead
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16(tbase + TM_D1, pd0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc_o,
@@ -786,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed && r5_pending && __syncthreads_or(!r5_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
-    if (nchunks > 0 && !failed && q < 2) store_o(nchunks - 1, T - (nchunks - 1) * kC);
+    if (nchunks > 0 && !failed && q >= 2) store_o(nchunks - 1, T - (nchunks - 1) * kC);
     // Final state -> hT.
     if (p.hT && !failed) {
         float* dst = p.hT + ((size_t)blockIdx.x * kD + lane) * kD + 32 * u;
