@@ -157,11 +157,11 @@ __device__ __forceinline__ uint64_t kstep_mnmajor(int kk) { return (uint64_t)(kk
 // the triangular inverse: tcgen05 needs M >= 64, these products are 16 x 16.
 // Fragment ownership (g = lane / 4, t = lane % 4): A rows g, g+8 and columns
 // t, t+4; B rows t, t+4 and column g; D rows g, g+8 and columns 2t, 2t+1.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// Operands are passed as their fp32 bits: the tensor core reads the TF32
+// fields and drops the low 13 mantissa bits (round toward zero, relative
+// error < 2^-10, below the bf16 rounding T' gets afterwards), which saves a
+// conversion per element on these instruction-bound steps.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
