@@ -80,6 +80,8 @@ constexpr uint32_t OFF_MS = OFF_FT + 64 * LDT * 4;  // fp32 level-2 slabs, 4 war
 constexpr int KM_ROWS = 160;                  // windows of 16, 32, 48, 64 rows
 __host__ __device__ __forceinline__ constexpr int win_row(int a) { return 8 * a * (a + 1); }
 static_assert(OFF_MS + 4 * 128 * 4 <= OFF_V, "solve scratch overflows the window buffer");
+static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 == 0,
+              "ldmatrix rows must start on 16-byte boundaries");
 
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
@@ -162,6 +164,20 @@ __device__ __forceinline__ uint64_t kstep_mnmajor(int kk) { return (uint64_t)(kk
 // error < 2^-10, below the bf16 rounding T' gets afterwards), which saves a
 // conversion per element on these instruction-bound steps.
 __device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x); }
+// The A fragment of one m16n8k8 TF32 MMA (rows R0.., columns K0.. of a
+// row-major fp32 matrix with leading dimension ld) in one ldmatrix.x4: seen as
+// b16 pairs, matrix j of the four 8x4-word tiles hands thread i the word at
+// (i / 4, i % 4), i.e. a[0..3] = (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4).
+// Rows must start on 16-byte boundaries (ld and K0 multiples of 4).
+__device__ __forceinline__ void ldsm_a_tf32(const float* m, int ld, int R0, int K0, int lane,
+                                            uint32_t* a) {
+    const int mat = lane >> 3, rr = lane & 7;
+    const float* p = m + (R0 + rr + 8 * (mat & 1)) * ld + K0 + 4 * (mat >> 1);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(smem_addr(p))
+                 : "memory");
+}
 __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
@@ -200,10 +216,8 @@ __device__ __forceinline__ void solve_level2(const float* FA, float* FT, float* 
 #pragma unroll
     for (int ks = 0; ks < 2; ks++) {  // M = A_{i,i-1} T_{i-1,i-1}[:, n0..]
         const int k0 = c0 + 8 * ks;
-        const uint32_t af[4] = {to_tf32(FA[(r0 + g) * LDA + k0 + t]),
-                                to_tf32(FA[(r0 + g + 8) * LDA + k0 + t]),
-                                to_tf32(FA[(r0 + g) * LDA + k0 + t + 4]),
-                                to_tf32(FA[(r0 + g + 8) * LDA + k0 + t + 4])};
+        uint32_t af[4];
+        ldsm_a_tf32(FA, LDA, r0, k0, lane, af);
         const uint32_t bf[2] = {to_tf32(FT[(k0 + t) * LDT + n0 + g]),
                                 to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
         mma_tf32(acc, af, bf);
@@ -215,10 +229,8 @@ __device__ __forceinline__ void solve_level2(const float* FA, float* FT, float* 
 #pragma unroll
     for (int ks = 0; ks < 2; ks++) {  // T_{i,i-1} = -T_ii M
         const int k0 = 8 * ks;
-        const uint32_t af[4] = {to_tf32(FT[(r0 + g) * LDT + r0 + k0 + t]),
-                                to_tf32(FT[(r0 + g + 8) * LDT + r0 + k0 + t]),
-                                to_tf32(FT[(r0 + g) * LDT + r0 + k0 + t + 4]),
-                                to_tf32(FT[(r0 + g + 8) * LDT + r0 + k0 + t + 4])};
+        uint32_t af[4];
+        ldsm_a_tf32(FT, LDT, r0, r0 + k0, lane, af);
         const uint32_t bf[2] = {to_tf32(M[(k0 + t) * 8 + g]), to_tf32(M[(k0 + t + 4) * 8 + g])};
         mma_tf32(out, af, bf);
     }
@@ -248,10 +260,8 @@ __device__ __forceinline__ void solve_level3(float* FA, const float* FT, int war
         for (int ks = 0; ks < 4; ks++) {
             if (ks < kb) continue;
             const int k0 = 8 * ks;
-            const uint32_t af[4] = {to_tf32(FA[(ra + g) * LDA + k0 + t]),
-                                    to_tf32(FA[(ra + g + 8) * LDA + k0 + t]),
-                                    to_tf32(FA[(ra + g) * LDA + k0 + t + 4]),
-                                    to_tf32(FA[(ra + g + 8) * LDA + k0 + t + 4])};
+            uint32_t af[4];
+            ldsm_a_tf32(FA, LDA, ra, k0, lane, af);
             const uint32_t bf[2] = {to_tf32(FT[(k0 + t) * LDT + n0 + g]),
                                     to_tf32(FT[(k0 + t + 4) * LDT + n0 + g])};
             mma_tf32(acc, af, bf);
@@ -267,10 +277,8 @@ __device__ __forceinline__ void solve_level3(float* FA, const float* FT, int war
     for (int ks = 0; ks < 4; ks++) {  // T_[23][01] = -T_[23][23] M
         if (ks >= 2 * (rt + 1)) break;
         const int k0 = 8 * ks;
-        const uint32_t af[4] = {to_tf32(FT[(r0 + g) * LDT + 32 + k0 + t]),
-                                to_tf32(FT[(r0 + g + 8) * LDT + 32 + k0 + t]),
-                                to_tf32(FT[(r0 + g) * LDT + 32 + k0 + t + 4]),
-                                to_tf32(FT[(r0 + g + 8) * LDT + 32 + k0 + t + 4])};
+        uint32_t af[4];
+        ldsm_a_tf32(FT, LDT, r0, 32 + k0, lane, af);
         const uint32_t bf[2] = {to_tf32(M[(k0 + t) * 8 + g]), to_tf32(M[(k0 + t + 4) * 8 + g])};
         mma_tf32(out, af, bf);
     }
