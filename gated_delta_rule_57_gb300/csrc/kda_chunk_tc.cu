@@ -20,13 +20,12 @@
 // Since W S0 = T' (Kt S0), the state enters only through Y = Kt S0 and
 // Qt S0, which need neither the Gram matrices nor the solve. As 128-row MMAs:
 //   round 1  Gram blocks  [Kp; Qp] * [Km_0; Km_1; Km_2; Km_3]^T   (N = 16+32+48+64)
-//   round A  D1  = [Kt; Qt] * S0                  -> [Y; Qt S0]   (runs under the solve)
+//   round 2  D1  = [Kt; Qt] * S0                  -> [Y; Qt S0]   (runs under the solve)
 //            V'  = V - Y  (bf16, in place of v; under the solve as well)
 //   round 3  SCR = [T'; P] * V'                   -> [U; -]      (U = Ut - W S0)
-//   round 5  S  += Kb^T * U                       (S pre-scaled by e^{G_C} in TMEM)
+//   round 4  S  += Kb^T * U                       (S pre-scaled by e^{G_C} in TMEM)
 //            D1 += [T'; P] * U                    -> [-; O]      (O = Qt S0 + P U)
-// The O rows are read out while the next chunk's round 1 runs. (Rounds 2
-// and 4 of earlier forms, X = P T' and [Qt; -W] S0, are gone.)
+// The O rows are read out while the next chunk's round 1 runs.
 //
 // Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
 // lane quarter), ~220 KB of shared memory (one CTA per SM), 416 TMEM columns:
@@ -50,9 +49,9 @@ using namespace ptx;
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
 constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
-// Round A is issued by warp 15, which has no other work during the solve
+// Round 2 is issued by warp 15, which has no other work during the solve
 // (issuing keeps a thread busy for about the MMA's duration).
-constexpr int kRoundAThread = kThreads - 32;
+constexpr int kRound2Thread = kThreads - 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (bytes from a 1024-aligned base).
@@ -68,7 +67,7 @@ constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
 constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
 constexpr uint32_t OFF_GT = 221952;    // fp32 [4][128] tile log2-decay totals
 constexpr uint32_t SMEM_BYTES = 224000 + 1024;
-// U (64 x 128, MN-major B) reuses [Kt; Qt] once round A has completed.
+// U (64 x 128, MN-major B) reuses [Kt; Qt] once round 2 has completed.
 constexpr uint32_t OFF_U = OFF_AKQ;
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
 // the solve)
@@ -86,7 +85,7 @@ static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 ==
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
 
-enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R5 = 4, BAR_RA = 5, NBAR = 6 };
+enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, NBAR = 6 };
 
 struct TcParams {
     const float* beta;
@@ -401,17 +400,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_phase ^= 1u;
         return ok;
     };
-    // Round 5 completes on its own barrier and is waited for only when its
+    // Round 4 completes on its own barrier and is waited for only when its
     // results (S, the O rows, the U and Kb operands' buffers) are next needed,
     // so the following chunk's decay scan and operand build run under it.
-    uint32_t r5_phase = 0, ra_phase = 0;
-    bool r5_pending = false;
-    auto r5_wait = [&]() {
+    uint32_t r4_phase = 0, r2_phase = 0;
+    bool r4_pending = false;
+    auto r4_wait = [&]() {
         bool ok = true;
-        if (r5_pending) {
-            ok = mbar_wait(&bars[BAR_R5], r5_phase);
-            r5_phase ^= 1u;
-            r5_pending = false;
+        if (r4_pending) {
+            ok = mbar_wait(&bars[BAR_R4], r4_phase);
+            r4_phase ^= 1u;
+            r4_pending = false;
         }
         tc_fence_after();
         return ok;
@@ -586,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
-        ok = r5_wait();  // Kb, U (under [Kt; Qt]), D1 and S are free again
+        ok = r4_wait();  // Kb, U (under [Kt; Qt]), D1 and S are free again
         if (!ok) flags |= KDA_DEV_TIMEOUT;
 #pragma unroll
         for (int e = 0; e < 2; e++) {
@@ -661,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
             unsigned char* TP = sm + OFF_A0;  // T' rows 0..63
-            if (tid == kRoundAThread) {
-                // Round A: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
+            if (tid == kRound2Thread) {
+                // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
                 const uint64_t ad0 = desc_kmajor(sbase + OFF_AKQ);
@@ -671,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk),
                              idesc, kk > 0);
-                mma_commit(&bars[BAR_RA]);
+                mma_commit(&bars[BAR_R2]);
             }
             if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
                 const int o0 = 16 * warp, jc = tid & 15;
@@ -709,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // V' = V - Y for token rows lane (0..63), value columns [64 hv, 64 hv + 64),
                 // in place of v, by the four warps that are idle in this level.
                 ok = mbar_wait(&bars[BAR_V], par);
-                ok = mbar_wait(&bars[BAR_RA], ra_phase) && ok;
+                ok = mbar_wait(&bars[BAR_R2], r2_phase) && ok;
                 tc_fence_after();
                 const int hv = (warp >> 2) & 1;
                 if (ok) {
@@ -729,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            ra_phase ^= 1u;
+            r2_phase ^= 1u;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -761,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // ------------------------------------------------------------ round 5: S += Kb^T U, O += P U
+        // ------------------------------------------------------------ round 4: S += Kb^T U, O += P U
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 128, 1, 1);
@@ -776,13 +775,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16(tbase + TM_D1, pd0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc_o,
                          1);
-            mma_commit(&bars[BAR_R5]);
+            mma_commit(&bars[BAR_R4]);
         }
-        r5_pending = true;
+        r4_pending = true;
         // Sparse state checkpoint: only full chunks count, so the slot index
         // stays below n_ckpt = T / ckpt_every.
         if (p.ckpt && (c + 1) % p.ck_chunks == 0 && (c + 1) / p.ck_chunks <= p.n_ckpt) {
-            if (__syncthreads_or(!r5_wait())) { failed = true; break; }
+            if (__syncthreads_or(!r4_wait())) { failed = true; break; }
             const int jc = (c + 1) / p.ck_chunks - 1;
             float* dst = p.ckpt + (((size_t)blockIdx.x * p.n_ckpt + jc) * kD + lane) * kD + 32 * u;
 #pragma unroll
@@ -798,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    if (!failed && r5_pending && __syncthreads_or(!r5_wait())) failed = true;
+    if (!failed && r4_pending && __syncthreads_or(!r4_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
     if (nchunks > 0 && !failed && q >= 2) store_o(nchunks - 1, T - (nchunks - 1) * kC);
