@@ -83,10 +83,20 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
 
 namespace {
 
+// Segments of a split sequence: ceil(chunks / nseg) chunks each, and the
+// number of non-empty segments that gives (at most nseg).
+void segment_shape(int T, int nseg, int* seg_chunks, int* nseg_eff) {
+    const int nch = (T + 63) / 64;
+    const int sc = nch > 0 ? (nch + nseg - 1) / nseg : 1;
+    *seg_chunks = sc;
+    *nseg_eff = nch > 0 ? (nch + sc - 1) / sc : 1;
+}
+
 kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B,
                             int T, int H, int dk, int dv, kda_dtype_t io, float* ckpt,
-                            int ckpt_every, int* d_status, void* stream) {
+                            int ckpt_every, int* d_status, void* stream, int nseg = 1,
+                            void* workspace = nullptr, size_t ws_bytes = 0) {
     if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
@@ -131,12 +141,38 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
                 return fail(KDA_ERR_INVALID_ARG, "ckpt overlaps another tensor");
     }
 
+    int seg_chunks = 0, nseg_eff = 1;
+    if (nseg != 1) {
+        if (io != KDA_BF16 || dk != 128)
+            return fail(KDA_ERR_UNSUPPORTED, "segmented prefill needs bf16 and dk = dv = 128");
+        const int nch = (T + 63) / 64;
+        if (nseg < 1 || (T > 0 && nseg > nch))
+            return fail(KDA_ERR_INVALID_ARG, "nseg must be in 1 .. ceil(T / 64)");
+        segment_shape(T, nseg, &seg_chunks, &nseg_eff);
+    }
+    if (nseg_eff > 1) {
+        const size_t need = kda::segmented_workspace_floats((long long)B * H, nseg_eff) * 4;
+        if (!workspace || ws_bytes < need)
+            return fail(KDA_ERR_WORKSPACE, "workspace smaller than the segmented size");
+        if (!aligned16(workspace))
+            return fail(KDA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        const void* all[] = {q, k, v, g, beta, h0, o, hT};
+        const size_t all_bytes[] = {n_qk * esz, n_qk * esz, n_v * esz, n_qk * 4, n_b * 4,
+                                    h0 ? n_s * 4 : 0, n_v * esz, hT ? n_s * 4 : 0};
+        for (int i = 0; i < 8; i++)
+            if (overlaps(workspace, need, all[i], all_bytes[i]))
+                return fail(KDA_ERR_INVALID_ARG, "workspace overlaps another tensor");
+    }
+
     kda::ChunkFwdArgs a{q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, d_status,
                         static_cast<cudaStream_t>(stream)};
     a.ckpt = ckpt;
     a.ckpt_every = ckpt ? ckpt_every : 0;
-    cudaError_t e = io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
-                                   : kda::launch_chunk_fwd_simt(a, io);
+    cudaError_t e = nseg_eff > 1
+                        ? kda::launch_chunk_fwd_tc_segmented(a, nseg_eff, seg_chunks,
+                                                             static_cast<float*>(workspace))
+                    : io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
+                                     : kda::launch_chunk_fwd_simt(a, io);
     if (e != cudaSuccess) {
         set_last_error(cudaGetErrorString(e));
         return KDA_ERR_CUDA;
@@ -165,6 +201,62 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
     if (!ckpt) return fail(KDA_ERR_INVALID_ARG, "ckpt must be non-NULL");
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, ckpt, ckpt_every,
                           d_status, stream);
+}
+
+int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t io) {
+    if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return -1;
+    if ((long long)B * H >= (1LL << 31)) return -1;
+    if (io != KDA_BF16 || dk != 128 || B == 0 || H == 0) return 1;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        nsm <= 0) {
+        cudaGetLastError();
+        return 1;
+    }
+    // Chunk-steps on the critical path with one sequence (or segment) per SM:
+    // whole sequences take ceil(BH / nsm) waves of nch chunks; nseg segments
+    // take the waves of the segment pass (BH * (2 nseg - 1) CTAs) and of the
+    // correction pass (BH * (nseg - 1)), each ceil(nch / nseg) chunks long.
+    const long long BH = (long long)B * H, nch = (T + 63) / 64;
+    auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
+    const long long base = waves(BH) * nch;
+    int best = 1;
+    long long best_cost = base;
+    for (int s = 2; s <= 32 && s <= nch; s++) {
+        int sc, se;
+        segment_shape(T, s, &sc, &se);
+        if (se != s) continue;
+        const long long cost = (waves(BH * (2 * s - 1)) + waves(BH * (s - 1))) * sc;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    // Segments cost extra work (three passes over the split part) and HBM
+    // traffic; take them only for a clear gain.
+    return best_cost * 5 < base * 4 ? best : 1;
+}
+
+size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int dv,
+                                              kda_dtype_t io, int nseg) {
+    if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return (size_t)-1;
+    if ((long long)B * H >= (1LL << 31)) return (size_t)-1;
+    const int nch = (T + 63) / 64;
+    if (nseg < 1 || (T > 0 && nseg > nch)) return (size_t)-1;
+    if (nseg > 1 && (io != KDA_BF16 || dk != 128)) return (size_t)-1;
+    int sc, se;
+    segment_shape(T, nseg, &sc, &se);
+    return se > 1 ? kda::segmented_workspace_floats((long long)B * H, se) * 4 : 0;
+}
+
+kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v,
+                                     const float* g, const float* beta, const float* h0, void* o,
+                                     float* hT, int B, int T, int H, int dk, int dv,
+                                     kda_dtype_t io, int nseg, void* workspace, size_t ws_bytes,
+                                     int* d_status, void* stream) {
+    return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0, d_status,
+                          stream, nseg, workspace, ws_bytes);
 }
 
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,

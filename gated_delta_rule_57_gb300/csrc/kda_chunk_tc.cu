@@ -97,6 +97,17 @@ struct TcParams {
     float* ckpt;    // [B, H, n_ckpt, dk, dv] or null
     int ck_chunks;  // chunks between checkpoints
     int n_ckpt;
+    // Segmented evaluation of long sequences (pass 0: one CTA per whole
+    // sequence). Pass 1: CTA i < BH * nseg runs segment i % nseg of sequence
+    // i / nseg from a zero state (segment 0 from h0), writing o and its final
+    // state to ws_s0; the next BH * (nseg - 1) CTAs run segments 1.. from the
+    // identity with v = 0, leaving the segment transition in ws_m. Pass 2:
+    // segments 1.. again from their incoming state ws_sin with v = 0, adding
+    // their outputs to o.
+    int pass, nseg, seg_chunks, BH;
+    float* ws_s0;         // [BH][nseg][dk][dv]
+    float* ws_m;          // [BH][nseg - 1][dk][dk]
+    const float* ws_sin;  // [BH][nseg - 1][dk][dv]
 };
 
 // 2^x on the SFU (ex2.approx, flush-to-zero). Arguments here are log2-decays
@@ -284,6 +295,9 @@ __device__ __forceinline__ void solve_level3(float* FA, const float* FT, int war
     store_tprime(TP, sbeta, r0 + g, n0 + 2 * t, out);
 }
 
+// SEG: the kernel serves the segment and correction passes (runtime task
+// decode); the whole-sequence instantiation compiles without any of it.
+template <bool SEG>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
@@ -301,9 +315,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMEM view of a warp: lane quarter q (lanes 32q..32q+31), column group u.
     const int q = warp & 3, u = warp >> 2;
     const int lane = 32 * q + (tid & 31);
-    const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int T = p.T;
-    const int nchunks = (T + kC - 1) / kC;
+    // This CTA's task (see TcParams): kind 0 runs a whole sequence or a segment
+    // from h0 / zero writing o, kind 1 a segment from the identity with v = 0
+    // (its transition), kind 2 a segment from its incoming state with v = 0,
+    // adding to o. Only kind and the first token stay live; the state
+    // pointers are formed where they are used.
+    const int kind =
+        !SEG ? 0 : p.pass == 2 ? 2 : ((p.pass == 1 && (int)blockIdx.x >= p.BH * p.nseg) ? 1 : 0);
+    const bool v_zero = kind != 0;
+    auto task_seq = [&](int* bh_out, int* seg_out) {
+        int bh = blockIdx.x, seg = 0;
+        if (kind == 2 || kind == 1) {
+            const int j = kind == 1 ? (int)blockIdx.x - p.BH * p.nseg : (int)blockIdx.x;
+            bh = j / (p.nseg - 1);
+            seg = 1 + j % (p.nseg - 1);
+        } else if (SEG && p.pass == 1) {
+            bh = blockIdx.x / p.nseg;
+            seg = blockIdx.x % p.nseg;
+        }
+        *bh_out = bh;
+        *seg_out = seg;
+    };
+    int bh, seg;
+    task_seq(&bh, &seg);
+    const int b = bh / p.H, h = bh % p.H;
+    const int t_begin = seg * p.seg_chunks * kC;
+    // Initial state: h0 (whole sequences and first segments), zero (other
+    // segments), the identity (transition runs) or the incoming state.
+    const float* h0p = kind == 2 ? p.ws_sin + ((size_t)bh * (p.nseg - 1) + seg - 1) * kD * kD
+                       : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * kD * kD
+                                                         : nullptr;
+    const int nchunks = (!SEG || p.pass == 0) ? (T + kC - 1) / kC
+                                              : min(p.seg_chunks, (T - t_begin + kC - 1) / kC);
     const uint32_t sbase = smem_addr(sm);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* slam = reinterpret_cast<float*>(sm + OFF_LAM);
@@ -333,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto issue_qk = [&](int c) {
         mbar_arrive_expect_tx(&bars[BAR_QK], 4 * 8192);
-        const int t0 = c * kC;
+        const int t0 = t_begin + c * kC;
         tma_load_4d(sm + OFF_KQP, &map_k, &bars[BAR_QK], 0, h, t0, b);
         tma_load_4d(sm + OFF_KQP + 16384, &map_k, &bars[BAR_QK], 64, h, t0, b);
         tma_load_4d(sm + OFF_KQP + 8192, &map_q, &bars[BAR_QK], 0, h, t0, b);
@@ -343,28 +387,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars[BAR_G], 32768);
 #pragma unroll
         for (int cbk = 0; cbk < 4; cbk++)
-            tma_load_4d(sm + OFF_G + cbk * 8192, &map_g, &bars[BAR_G], 32 * cbk, h, c * kC, b);
+            tma_load_4d(sm + OFF_G + cbk * 8192, &map_g, &bars[BAR_G], 32 * cbk, h, t_begin + c * kC,
+                        b);
     };
     auto issue_v = [&](int c) {
         mbar_arrive_expect_tx(&bars[BAR_V], 2 * 8192);
-        tma_load_4d(sm + OFF_V, &map_v, &bars[BAR_V], 0, h, c * kC, b);
-        tma_load_4d(sm + OFF_V + 8192, &map_v, &bars[BAR_V], 64, h, c * kC, b);
+        tma_load_4d(sm + OFF_V, &map_v, &bars[BAR_V], 0, h, t_begin + c * kC, b);
+        tma_load_4d(sm + OFF_V + 8192, &map_v, &bars[BAR_V], 64, h, t_begin + c * kC, b);
     };
     if (tid == 0 && nchunks > 0) {
         issue_qk(0);
         issue_g(0);
-        issue_v(0);
+        if (!v_zero) issue_v(0);
     }
     // beta is strided by H in memory: plain loads, kept one chunk ahead.
     auto load_beta = [&](int c) {
-        const int t = c * kC + tid;
+        const int t = t_begin + c * kC + tid;
         return (tid < kC && c < nchunks && t < T) ? p.beta[((size_t)b * T + t) * p.H + h] : 0.f;
     };
     float beta_next = load_beta(0);
 
     // Incoming state -> TMEM (lane i = key channel i, column j = value channel j).
     {
-        const float* src = p.h0 ? p.h0 + ((size_t)blockIdx.x * kD + lane) * kD + 32 * u : nullptr;
+        const float* src = h0p ? h0p + (size_t)lane * kD + 32 * u : nullptr;
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 16) {
             float x[16];
@@ -373,6 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float4 f = src ? *reinterpret_cast<const float4*>(src + cc + j)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
+            }
+            if (kind == 1) {
+#pragma unroll
+                for (int j = 0; j < 16; j++) x[j] = (lane == 32 * u + cc + j) ? 1.f : 0.f;
             }
             tmem_st16(tq + TM_S + 32 * u + cc, x);
         }
@@ -384,13 +433,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // O rows of chunk cc (D1 lanes 64..127, columns [32u, 32u + 32)) -> global.
     auto store_o = [&](int cc, int len) {
+        if (kind == 1) return;
         float x[32];
         tmem_ld32(tq + TM_D1 + 32 * u, x);
         if (lane - 64 < len) {
             __nv_bfloat16* dst =
-                p.o + (((size_t)b * T + cc * kC + lane - 64) * p.H + h) * kD + 32 * u;
+                p.o + (((size_t)b * T + t_begin + cc * kC + lane - 64) * p.H + h) * kD + 32 * u;
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
+            for (int e = 0; e < 32; e += 8) {
+                if (kind == 2) {  // o += this pass's contribution
+                    float prev[8];
+                    unpack8(*reinterpret_cast<const uint4*>(dst + e), prev);
+#pragma unroll
+                    for (int z = 0; z < 8; z++) x[e + z] += prev[z];
+                }
+                *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
+            }
         }
     };
 
@@ -707,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp >= 8 && q < 2) {
                 // V' = V - Y for token rows lane (0..63), value columns [64 hv, 64 hv + 64),
                 // in place of v, by the four warps that are idle in this level.
-                ok = mbar_wait(&bars[BAR_V], par);
+                ok = v_zero || mbar_wait(&bars[BAR_V], par);
                 ok = mbar_wait(&bars[BAR_R2], r2_phase) && ok;
                 tc_fence_after();
                 const int hv = (warp >> 2) & 1;
@@ -719,8 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(tq + TM_D1 + c0, y);
 #pragma unroll
                         for (int e = 0; e < 32; e += 8) {
-                            float vv[8];
-                            ld_row8(sm + OFF_V, lane, c0 + e, 64, vv);
+                            float vv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (!v_zero) ld_row8(sm + OFF_V, lane, c0 + e, 64, vv);
 #pragma unroll
                             for (int z = 0; z < 8; z++) vv[z] -= y[e + z];
                             st_row8(sm + OFF_V, lane, c0 + e, 64, vv);
@@ -749,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mma_wait();
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
+        if (tid == 0 && c + 1 < nchunks && !v_zero) issue_v(c + 1);
         if (q < 2) {  // U rows (scratch lanes 0..63) -> bf16 operand
             float x[32];
             tmem_ld32(tq + TM_SCR + 32 * u, x);
@@ -800,10 +858,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed && r4_pending && __syncthreads_or(!r4_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
-    if (nchunks > 0 && !failed && q >= 2) store_o(nchunks - 1, T - (nchunks - 1) * kC);
+    if (nchunks > 0 && !failed && q >= 2)
+        store_o(nchunks - 1, min(kC, T - t_begin - (nchunks - 1) * kC));
     // Final state -> hT.
-    if (p.hT && !failed) {
-        float* dst = p.hT + ((size_t)blockIdx.x * kD + lane) * kD + 32 * u;
+    // Final state: hT (whole sequences), the segment's zero-start state or
+    // its transition (segment pass), nothing (correction pass).
+    float* hTp = nullptr;
+    {
+        int bh2, seg2;
+        task_seq(&bh2, &seg2);
+        if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * kD * kD : nullptr;
+        else if (kind == 0) hTp = p.ws_s0 + ((size_t)bh2 * p.nseg + seg2) * kD * kD;
+        else if (kind == 1) hTp = p.ws_m + ((size_t)bh2 * (p.nseg - 1) + seg2 - 1) * kD * kD;
+    }
+    if (hTp && !failed) {
+        float* dst = hTp + (size_t)lane * kD + 32 * u;
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 16) {
             float x[16];
@@ -852,25 +921,74 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, 
 
 }  // namespace
 
-cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
-    if (a.dk != kD || a.dv != kD) return launch_chunk_fwd_simt(a, KDA_BF16);
+namespace {
+
+struct TcMaps {
+    CUtensorMap q{}, k{}, v{}, g{};
+};
+
+bool make_maps(TcMaps* m, const ChunkFwdArgs& a) {
+    if (a.T == 0) return true;
+    return make_map(&m->q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
+           make_map(&m->k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
+           make_map(&m->v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
+           make_map(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.H, kD, 32);
+}
+
+TcParams base_params(const ChunkFwdArgs& a) {
     TcParams p{a.beta, a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.T, a.H, a.d_status,
                a.ckpt, a.ckpt ? a.ckpt_every / kC : 1, a.ckpt ? a.T / a.ckpt_every : 0};
-    CUtensorMap mq{}, mk{}, mv{}, mg{};
-    if (a.T > 0) {
-        const int T = a.T;
-        if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64) ||
-            !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64) ||
-            !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, T, a.H, kD, 64) ||
-            !make_map(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, T, a.H, kD, 32))
-            return cudaErrorInvalidValue;
-    }
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel,
+    p.pass = 0;
+    p.nseg = 1;
+    p.seg_chunks = 0;
+    p.BH = a.B * a.H;
+    p.ws_s0 = p.ws_m = nullptr;
+    p.ws_sin = nullptr;
+    return p;
+}
+
+template <bool SEG>
+cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel<SEG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((long long)a.B * a.H);
-    kda_chunk_tc_kernel<<<grid, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
+    kda_chunk_tc_kernel<SEG><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.g, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
+    if (a.dk != kD || a.dv != kD) return launch_chunk_fwd_simt(a, KDA_BF16);
+    TcMaps m;
+    if (!make_maps(&m, a)) return cudaErrorInvalidValue;
+    return launch_tc<false>(m, base_params(a), (long long)a.B * a.H, a.stream);
+}
+
+cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int seg_chunks,
+                                          float* ws) {
+    if (nseg <= 1) return launch_chunk_fwd_tc(a);
+    TcMaps m;
+    if (!make_maps(&m, a)) return cudaErrorInvalidValue;
+    const long long BH = (long long)a.B * a.H;
+    const size_t DD = (size_t)kD * kD;
+    float* s0 = ws;
+    float* mt = s0 + (size_t)BH * nseg * DD;
+    float* sin = mt + (size_t)BH * (nseg - 1) * DD;
+    TcParams p = base_params(a);
+    p.nseg = nseg;
+    p.seg_chunks = seg_chunks;
+    p.ws_s0 = s0;
+    p.ws_m = mt;
+    p.ws_sin = sin;
+    p.hT = nullptr;  // the final state comes out of the scan
+    p.pass = 1;
+    cudaError_t e = launch_tc<true>(m, p, BH * (2 * nseg - 1), a.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_segment_scan(s0, mt, sin, a.hT, (int)BH, nseg, a.stream);
+    if (e != cudaSuccess) return e;
+    p.pass = 2;
+    return launch_tc<true>(m, p, BH * (nseg - 1), a.stream);
 }
 
 }  // namespace kda

@@ -79,6 +79,13 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_chunk_fwd_ckpt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I,
                                              I, vp, vp]
             L.kda_chunk_fwd_ckpt.restype = I
+            L.kda_chunk_fwd_segmented.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I,
+                                                  I, I, vp, sz, vp, vp]
+            L.kda_chunk_fwd_segmented.restype = I
+            L.kda_chunk_fwd_segmented_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            L.kda_chunk_fwd_segmented_workspace_size.restype = sz
+            L.kda_chunk_fwd_segments_hint.argtypes = [I, I, I, I, I, I]
+            L.kda_chunk_fwd_segments_hint.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
             L.kda_decode_step.restype = I
             L.kda_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I,
@@ -146,6 +153,51 @@ def kda_chunk_fwd(q, k, v, g, beta, h0=None, *, o=None, hT=None, want_hT: bool =
     code = lib().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                _ptr(o), _ptr(hT), B, T, H, dk, dv, io, _ptr(workspace),
                                ws_bytes, _ptr(status), _stream(stream))
+    _check(code)
+    return o, hT
+
+
+def kda_chunk_fwd_segments_hint(B: int, T: int, H: int, dk: int, dv: int,
+                                io: torch.dtype = torch.bfloat16) -> int:
+    """Recommended segment count for kda_chunk_fwd_segmented on this device."""
+    n = lib().kda_chunk_fwd_segments_hint(B, T, H, dk, dv, _DTYPE[io])
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size")
+    return int(n)
+
+
+def kda_chunk_fwd_segmented_workspace_size(B: int, T: int, H: int, dk: int, dv: int,
+                                           io: torch.dtype = torch.bfloat16,
+                                           nseg: int = 1) -> int:
+    n = lib().kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, _DTYPE[io], nseg)
+    if n == ctypes.c_size_t(-1).value:
+        raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size or segment count")
+    return int(n)
+
+
+def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg: Optional[int] = None, o=None,
+                            hT=None, want_hT: bool = True, status: Optional[torch.Tensor] = None,
+                            workspace=None, stream=None):
+    """kda_chunk_fwd with each sequence split in time into `nseg` segments run
+    in parallel (None: the library's hint for this device). Returns (o, hT)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if nseg is None:
+        nseg = kda_chunk_fwd_segments_hint(B, T, H, dk, dv, q.dtype)
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, q.dtype, nseg)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().kda_chunk_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                         _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, io, nseg,
+                                         _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check(code)
     return o, hT
 

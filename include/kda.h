@@ -141,6 +141,58 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
                                 kda_dtype_t io, int* d_status, void* stream);
 
 /*
+ * kda_chunk_fwd with every sequence split in time into segments that run in
+ * parallel, for few long sequences (B * H well below the SM count). Section
+ * "The bill arrives in the serving stack", first bullet: the incoming state
+ * of a segment is not a sum of per-segment states, but each segment has two
+ * composable summaries, its cumulative transition M (the product of its
+ * per-token transitions) and its final state S0 from a zero start, and a
+ * prefix scan over them rebuilds every segment's incoming state. Here: a
+ * segment pass (every segment from a zero start, the first from h0, writing
+ * o; segments after the first also from the identity with v = 0, giving M),
+ * the scan X_{s+1} = S0_s + M_s X_s in fp32 (its last value is hT), and a
+ * correction pass (segments after the first again, from X_s with v = 0,
+ * adding their outputs to o). o and hT equal kda_chunk_fwd's up to rounding
+ * (o of later segments is the sum of two bf16-rounded parts).
+ *
+ *   nseg      : segments per sequence, 1 .. ceil(T / 64); segments are
+ *               ceil(ceil(T / 64) / nseg) chunks of 64 tokens (the last may
+ *               be shorter, and fewer segments result when chunks run out);
+ *               1 runs kda_chunk_fwd
+ *   workspace : device buffer of kda_chunk_fwd_segmented_workspace_size bytes,
+ *               16-byte aligned, not overlapping any other tensor; contents
+ *               are scratch
+ *
+ * Other arguments as for kda_chunk_fwd. Needs io = KDA_BF16 and
+ * dk = dv = 128 when it splits (KDA_ERR_UNSUPPORTED otherwise); a missing or
+ * short workspace returns KDA_ERR_WORKSPACE. The split part costs about three
+ * times the arithmetic of one pass; kda_chunk_fwd_segments_hint says when it
+ * pays.
+ */
+kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v,
+                                     const float* g, const float* beta, const float* h0, void* o,
+                                     float* hT, int B, int T, int H, int dk, int dv,
+                                     kda_dtype_t io, int nseg, void* workspace, size_t ws_bytes,
+                                     int* d_status, void* stream);
+
+/*
+ * Bytes of workspace kda_chunk_fwd_segmented needs: (3 nseg' - 2) * dk * dv * 4
+ * per (b, h), nseg' the number of segments that results, 0 when that is 1.
+ * Returns (size_t)-1 for arguments kda_chunk_fwd_segmented would reject.
+ */
+size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int dv,
+                                              kda_dtype_t io, int nseg);
+
+/*
+ * Segment count that minimises the number of chunk steps on the critical
+ * path on the current device (one CTA per SM, whole sequences against the
+ * segment and correction passes), or 1 when splitting does not save at
+ * least a fifth; 1 also when no CUDA device is visible or the configuration
+ * has no segmented path. -1 for arguments kda_chunk_fwd would reject.
+ */
+int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t io);
+
+/*
  * One decode step for N sequences (one token each), state updated in place
  * (section "The bill arrives in the serving stack", third bullet: the state
  * is overwritten where it lives).

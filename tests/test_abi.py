@@ -149,3 +149,49 @@ def call_ckpt(L, ckpt=A[7], every=128, T=256, **kw):
 ])
 def test_chunk_fwd_ckpt_rejects(L, kw, code):
     assert call_ckpt(L, **kw) == code
+
+
+def test_segmented_workspace_size(L):
+    sz = ctypes.c_size_t(-1).value
+    f = L.kda_chunk_fwd_segmented_workspace_size
+    f.restype = ctypes.c_size_t
+    per = 128 * 128 * 4
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 5) == 32 * 13 * per  # 64 chunks -> 5 x 13
+    assert f(2, 640, 3, 128, 128, kda.KDA_BF16, 10) == 6 * 28 * per    # one chunk each
+    assert f(1, 1000, 2, 128, 128, kda.KDA_BF16, 7) == 2 * 16 * per    # 16 chunks -> 6 x 3
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 1) == 0
+    assert f(1, 64, 1, 128, 128, kda.KDA_BF16, 1) == 0
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 0) == sz
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 65) == sz             # more segments than chunks
+    assert f(1, 4096, 32, 128, 128, kda.KDA_F32, 2) == sz               # no segmented fp32 path
+    assert f(1, 4096, 32, 64, 64, kda.KDA_BF16, 2) == sz
+    assert f(-1, 4096, 32, 128, 128, kda.KDA_BF16, 2) == sz
+
+
+def test_segments_hint(L):
+    n = L.kda_chunk_fwd_segments_hint(1, 1 << 20, 32, 128, 128, kda.KDA_BF16)
+    assert 1 <= n <= 32  # 1 without a visible GPU
+    assert L.kda_chunk_fwd_segments_hint(1, 4096, 32, 128, 128, kda.KDA_F32) == 1
+    assert L.kda_chunk_fwd_segments_hint(1, 4096, 32, 96, 96, kda.KDA_BF16) == -1
+    assert L.kda_chunk_fwd_segments_hint(-1, 4096, 32, 128, 128, kda.KDA_BF16) == -1
+
+
+def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A[0]):
+    # T = 128: two chunks; every tensor fits the 64 KB spacing of the fake addresses
+    return L.kda_chunk_fwd_segmented(q, A[1], A[2], A[3], A[4], None, A[5], A[6], 1, T, 1, dk,
+                                     dk, io, nseg, ws, ws_bytes, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nseg=0), ST.KDA_ERR_INVALID_ARG),
+    (dict(nseg=3), ST.KDA_ERR_INVALID_ARG),                       # 2 chunks
+    (dict(io=kda.KDA_F32), ST.KDA_ERR_UNSUPPORTED),
+    (dict(dk=64), ST.KDA_ERR_UNSUPPORTED),
+    (dict(ws=None, ws_bytes=0), ST.KDA_ERR_WORKSPACE),
+    (dict(ws=A[7], ws_bytes=1024), ST.KDA_ERR_WORKSPACE),         # short
+    (dict(ws=A[7] + 8, ws_bytes=1 << 22), ST.KDA_ERR_INVALID_ARG),  # misaligned
+    (dict(ws=A[0], ws_bytes=1 << 22), ST.KDA_ERR_INVALID_ARG),    # overlaps q
+    (dict(q=None), ST.KDA_ERR_INVALID_ARG),
+])
+def test_segmented_rejects(L, kw, code):
+    assert call_seg(L, **kw) == code
