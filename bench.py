@@ -8,7 +8,9 @@ dk=dv=128 (bf16 q/k/v/o, fp32 g/beta/states, h0 ~ N(0, 0.02^2), hT returned).
 The same run also times the batched decode workload (256 sequences x H=32,
 128x128 fp32 state updated in place, 1000 consecutive steps) and reports it
 in the "decode" object, and a speculative-decoding round (verify + commit of 4
-draft tokens) in "spec_decode". Inputs are synthetic (seeded), already
+draft tokens) in "spec_decode", and the long-context workload (B=1, T=2^20,
+H=32) single-pass and split in time into parallel segments in "prefill_long"
+(--no-long skips it). Inputs are synthetic (seeded), already
 resident in HBM for `value`; `e2e` repeats the prefill step through the same
 C-ABI call from pinned host buffers, every input uploaded and o, hT read back
 inside the timed region, pipelined by batch row over copy and compute streams.
@@ -355,6 +357,47 @@ def time_spec_decode(device, seed, K=4, iters=50, warmup=5):
     return a.elapsed_time(b) / iters, iters * 2
 
 
+def time_prefill_long(device, seed, iters=3, warmup=1):
+    """The long-context workload (B=1, T=2^20, H=32): 32 sequences leave most
+    SMs idle in one pass, so it is also run split in time into the segment
+    count kda_chunk_fwd_segments_hint picks (segment pass, scan, correction).
+    Returns (single-pass ms, segmented ms, nseg, launches per segmented call)."""
+    from gated_delta_rule_57_gb300 import kda
+    w = inputs.PREFILL_T1M
+    x = inputs.prefill_inputs(w, device, seed=seed)
+    o = torch.empty_like(x["v"])
+    hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=device)
+    nseg = kda.kda_chunk_fwd_segments_hint(w.B, w.T, w.H, w.dk, w.dv)
+    ws = torch.empty(max(1, kda.kda_chunk_fwd_segmented_workspace_size(
+        w.B, w.T, w.H, w.dk, w.dv, nseg=nseg)), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def single():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, o=o, hT=hT,
+                          stream=stream)
+
+    def segmented():
+        kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], None, nseg=nseg,
+                                    o=o, hT=hT, workspace=ws, stream=stream)
+
+    res = []
+    for f in (single, segmented):
+        for _ in range(warmup):
+            f()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            f()
+        b.record(stream)
+        torch.cuda.synchronize()
+        res.append(a.elapsed_time(b) / iters)
+    del x, o, ws
+    torch.cuda.empty_cache()
+    return res[0], res[1], nseg, (3 if nseg > 1 else 1)
+
+
 def oracle_sample(budget_s, max_b=None):
     """Oracle on whole batch rows of the prefill workload until ~budget_s."""
     import oracle
@@ -416,6 +459,27 @@ def run_ours(args):
     spec_b = spec_bytes(DECODE, 4)
     spec_gbs = job_value(spec_b, max_over_ranks(spec_ms, world, device), world) / 1e9
 
+    long_obj = None
+    if not args.no_long:
+        wl = inputs.PREFILL_T1M
+        l1_ms, ls_ms, l_nseg, l_launch = time_prefill_long(device, rank_seed(wl.seed, rank))
+        l1_ms = max_over_ranks(l1_ms, world, device)
+        ls_ms = max_over_ranks(ls_ms, world, device)
+        l_bytes = prefill_bytes(wl)
+        l_tok = wl.B * wl.T
+        long_obj = {
+            "workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H,
+            "single_pass": {"ms_per_step": l1_ms, "value": job_value(l_tok, l1_ms, world),
+                            "unit": "tokens/s",
+                            "frac_of_peak_hbm": l_bytes / (l1_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+            "segmented": {"nseg": l_nseg, "ms_per_step": ls_ms,
+                          "value": job_value(l_tok, ls_ms, world), "unit": "tokens/s",
+                          "frac_of_peak_hbm": l_bytes / (ls_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "launches_per_step": l_launch},
+            "speedup": l1_ms / ls_ms,
+            "algorithmic_bytes_per_step": l_bytes,
+        }
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -464,6 +528,7 @@ def run_ours(args):
                             "algorithmic_bytes_per_round": spec_b,
                             "tokens_per_s": world * DECODE.N * 4 / (spec_ms * 1e-3),
                             "gpu_launches": spec_launches},
+            "prefill_long": long_obj,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -513,6 +578,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the T = 2^20 long-context measurement (52 GB of inputs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":
