@@ -81,6 +81,12 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
 
 }  // extern "C"
 
+// Scratch of kda_chunk_fwd_segmented_noalloc: 48 MB in the library's own
+// device image (one instance per device, set up when the module loads), so
+// that entry point allocates nothing. It holds the (3 nseg - 2) 64 KB states
+// per sequence of e.g. 32 sequences x 8 segments.
+static __device__ __align__(256) float g_seg_scratch[12u << 20];
+
 namespace {
 
 // Segments of a split sequence: ceil(chunks / nseg) chunks each, and the
@@ -257,6 +263,30 @@ kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v
                                      int* d_status, void* stream) {
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0, d_status,
                           stream, nseg, workspace, ws_bytes);
+}
+
+kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
+                                             const float* g, const float* beta, const float* h0,
+                                             void* o, float* hT, int B, int T, int H, int dk,
+                                             int dv, kda_dtype_t io, int nseg, int* d_status,
+                                             void* stream) {
+    const size_t need = kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, io, nseg);
+    if (need == (size_t)-1)  // the full call reports which argument is wrong
+        return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0,
+                              d_status, stream, nseg, nullptr, 0);
+    if (need > sizeof(g_seg_scratch))
+        return fail(KDA_ERR_WORKSPACE, "problem needs more than the static segment scratch");
+    void* ws = nullptr;
+    if (need > 0) {
+        // the array has one instance per device: take the current device's
+        cudaError_t e = cudaGetSymbolAddress(&ws, g_seg_scratch);
+        if (e != cudaSuccess) {
+            set_last_error(cudaGetErrorString(e));
+            return KDA_ERR_CUDA;
+        }
+    }
+    return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0, d_status,
+                          stream, nseg, ws, need > 0 ? sizeof(g_seg_scratch) : 0);
 }
 
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,

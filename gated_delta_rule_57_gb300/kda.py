@@ -84,6 +84,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_chunk_fwd_segmented.restype = I
             L.kda_chunk_fwd_segmented_workspace_size.argtypes = [I, I, I, I, I, I, I]
             L.kda_chunk_fwd_segmented_workspace_size.restype = sz
+            L.kda_chunk_fwd_segmented_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I,
+                                                          I, I, I, I, I, vp, vp]
+            L.kda_chunk_fwd_segmented_noalloc.restype = I
             L.kda_chunk_fwd_segments_hint.argtypes = [I, I, I, I, I, I]
             L.kda_chunk_fwd_segments_hint.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
@@ -198,6 +201,26 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg: Optional[int] = 
     code = lib().kda_chunk_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                          _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, io, nseg,
                                          _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+    _check(code)
+    return o, hT
+
+
+def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, h0=None, *, nseg: int, o=None,
+                                    hT=None, want_hT: bool = True,
+                                    status: Optional[torch.Tensor] = None, stream=None):
+    """kda_chunk_fwd_segmented with the library's static scratch (no workspace)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    code = lib().kda_chunk_fwd_segmented_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                                 _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, io,
+                                                 nseg, _ptr(status), _stream(stream))
     _check(code)
     return o, hT
 

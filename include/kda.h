@@ -184,6 +184,21 @@ size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int d
                                               kda_dtype_t io, int nseg);
 
 /*
+ * kda_chunk_fwd_segmented with the scratch in a fixed 48 MB device array of
+ * the library (one per device; its address is taken on the current device at
+ * each call), so the call allocates nothing and takes no workspace argument.
+ * Problems whose kda_chunk_fwd_segmented_workspace_size exceeds 48 MB return
+ * KDA_ERR_WORKSPACE before any launch. The array is shared by every call on
+ * a device: calls must not run concurrently on different streams of the
+ * same device. Other arguments and errors as for kda_chunk_fwd_segmented.
+ */
+kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
+                                             const float* g, const float* beta, const float* h0,
+                                             void* o, float* hT, int B, int T, int H, int dk,
+                                             int dv, kda_dtype_t io, int nseg, int* d_status,
+                                             void* stream);
+
+/*
  * Segment count that minimises the number of chunk steps on the critical
  * path on the current device (one CTA per SM, whole sequences against the
  * segment and correction passes), or 1 when splitting does not save at
