@@ -295,7 +295,8 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
     if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
-    if ((long long)N * H >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "N*H too large");
+    // two blocks per (sequence, head)
+    if ((long long)N * H * 2 >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "N*H too large");
     if (N == 0 || H == 0) return KDA_OK;
     if (!q || !k || !v || !g || !beta || !S || !o)
         return fail(KDA_ERR_INVALID_ARG, "all decode pointers must be non-NULL");

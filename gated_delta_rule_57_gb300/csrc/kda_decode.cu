@@ -9,42 +9,49 @@
 // The last identity lets both reductions over the key channel (S'^T k and
 // S'^T q) share one pass over S, so S is read once and written once.
 //
-// Memory plan. One CTA per (sequence, head). The dk x dv fp32 state (64 KB at
-// d = 128) is read with 16-byte loads, fully coalesced (a warp reads one
-// 512-byte row), kept in registers across the reduction, and written back in
-// place from the same registers. The kernel is bound by HBM bandwidth:
-// 2 * dk * dv * 4 bytes of state traffic per head against ~5 flops per state
-// element.
+// Memory plan. Two CTAs per (sequence, head), each owning half of the value
+// columns (the columns of S evolve independently given k, g, beta); the two
+// halves of a head are adjacent blocks. Each CTA's half of the dk x dv fp32
+// state (32 KB at d = 128) is read with 16-byte loads (a warp reads two
+// 256-byte row halves), kept in registers across the reduction (16 rows x 4
+// columns per thread), and written back in place from the same registers.
+// Small CTAs (four per SM) keep one another's loads, arithmetic and stores
+// overlapped. The kernel is bound by HBM bandwidth: 2 * dk * dv * 4 bytes of
+// state traffic per head against ~5 flops per state element.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-template <typename TIn, int DK, int DV, int NT>
-__global__ void __launch_bounds__(NT, 2)
+// DVS: value columns per CTA (a slice of the DV columns of a head; the
+// slices of one head are adjacent blocks).
+template <typename TIn, int DK, int DV, int DVS, int NT>
+__global__ void __launch_bounds__(NT, 512 / NT)
     kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                       const TIn* __restrict__ v, const float* __restrict__ g,
                       const float* __restrict__ beta, float* __restrict__ S,
                       TIn* __restrict__ o, int* __restrict__ d_status) {
-    constexpr int CG = DV / 4;         // float4 column groups per row
+    constexpr int CG = DVS / 4;        // float4 column groups per row slice
     constexpr int RG = NT / CG;        // row groups (rows handled in parallel)
     constexpr int RPT = DK / RG;       // rows per thread
     constexpr int NW = NT / 32;
     static_assert(NT % CG == 0 && DK % RG == 0, "bad decode tiling");
 
     __shared__ float s_k[DK], s_q[DK], s_a[DK];
-    __shared__ float s_red[2][RG][DV];
+    __shared__ float s_red[2][RG][DVS];
     __shared__ float s_kq[NW];
 
     const int tid = threadIdx.x;
-    const size_t head = blockIdx.x;  // n * H + h
+    constexpr int NS = DV / DVS;
+    const size_t head = blockIdx.x / NS;  // n * H + h
+    const int j0 = (int)(blockIdx.x % NS) * DVS;
     const int cg = tid % CG, rg = tid / CG;
-    float4* Sh = reinterpret_cast<float4*>(S + head * DK * DV);
+    float4* Sh = reinterpret_cast<float4*>(S + head * DK * DV + j0);
 
     // Issue the state loads first: they are the bulk of the traffic.
     float4 st[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; r++) st[r] = Sh[(size_t)(rg + r * RG) * CG + cg];
+    for (int r = 0; r < RPT; r++) st[r] = Sh[(size_t)(rg + r * RG) * (DV / 4) + cg];
 
     int flags = 0;
     float kq = 0.f;
@@ -106,8 +113,8 @@ __global__ void __launch_bounds__(NT, 2)
             kvj += s_red[0][w][j];
             qvj += s_red[1][w][j];
         }
-        u[c] = b * (to_f32(v[head * DV + j]) - kvj);
-        if (rg == 0) o[head * DV + j] = from_f32<TIn>(qvj + u[c] * kqt);
+        u[c] = b * (to_f32(v[head * DV + j0 + j]) - kvj);
+        if (rg == 0) o[head * DV + j0 + j] = from_f32<TIn>(qvj + u[c] * kqt);
     }
 
     // S = S' + k u^T, written back in place.
@@ -118,15 +125,15 @@ __global__ void __launch_bounds__(NT, 2)
         st[r].y += ki * u[1];
         st[r].z += ki * u[2];
         st[r].w += ki * u[3];
-        Sh[(size_t)(rg + r * RG) * CG + cg] = st[r];
+        Sh[(size_t)(rg + r * RG) * (DV / 4) + cg] = st[r];
     }
 }
 
 template <typename TIn, int D>
 cudaError_t launch_t(const DecodeArgs& a) {
-    constexpr int NT = 256;
-    const unsigned grid = (unsigned)((long long)a.N * a.H);
-    kda_decode_kernel<TIn, D, D, NT><<<grid, NT, 0, a.stream>>>(
+    constexpr int DVS = D / 2, NT = D;  // two CTAs per head, 16 rows x 4 columns per thread
+    const unsigned grid = (unsigned)((long long)a.N * a.H * (D / DVS));
+    kda_decode_kernel<TIn, D, D, DVS, NT><<<grid, NT, 0, a.stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
         static_cast<const TIn*>(a.v), a.g, a.beta, a.S, static_cast<TIn*>(a.o), a.d_status);
     return cudaGetLastError();

@@ -31,7 +31,7 @@
  *     1/sqrt(dk) pre-scale q.
  *   - Supported sizes: dk = dv in {64, 128}; any T >= 0 (ragged tails are
  *     handled; T = 0 writes hT = h0); B, H, N >= 0 (zero launches nothing)
- *     with B*H, N*H < 2^31 and every tensor under 2^62 elements.
+ *     with B*H < 2^31, N*H < 2^30 and every tensor under 2^62 elements.
  *
  * Errors
  *   - Argument errors are reported synchronously by the return value and

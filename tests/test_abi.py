@@ -104,6 +104,7 @@ def call_dec(L, q=A[0], k=A[1], v=A[2], g=A[3], beta=A[4], S=A[5], o=A[6], N=2, 
     (dict(o=A[2]), ST.KDA_ERR_INVALID_ARG),
     (dict(S=A[5] + 4), ST.KDA_ERR_INVALID_ARG),
     (dict(io=3), ST.KDA_ERR_INVALID_ARG),
+    (dict(N=1 << 15, H=1 << 15), ST.KDA_ERR_INVALID_ARG),  # 2 N H blocks >= 2^31
 ])
 def test_decode_rejects(L, kw, code):
     assert call_dec(L, **kw) == code
