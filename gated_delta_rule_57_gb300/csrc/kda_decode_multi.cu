@@ -25,7 +25,7 @@ namespace {
 // its own v columns. Small CTAs let several per SM overlap one CTA's per-token
 // reductions with another's state streaming.
 template <typename TIn, int DK, int DVS, int NT>
-__global__ void __launch_bounds__(NT, 384 / NT)
+__global__ void __launch_bounds__(NT, 512 / NT)
     kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                             const TIn* __restrict__ v, const float* __restrict__ g,
                             const float* __restrict__ beta, float* __restrict__ S,
