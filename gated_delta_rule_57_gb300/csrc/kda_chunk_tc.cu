@@ -33,9 +33,11 @@
 // whole sequence. Inputs arrive by TMA with the 128-byte swizzle (q, k, v in
 // the layout the MMA descriptors expect; g in 32-channel blocks); the next
 // chunk's g, q/k, v and beta are prefetched as soon as their buffers are free.
-// One thread issues the MMAs; completion is signalled through mbarriers whose
-// waits are bounded (timeout -> KDA_DEV_TIMEOUT). Intermediates never leave
-// the SM: the kernel reads each input once and writes o (and hT) once.
+// Thread 0 issues rounds 1, 3 and 4, a thread of warp 15 round 2; completion
+// is signalled through mbarriers whose waits are bounded (timeout ->
+// KDA_DEV_TIMEOUT). Intermediates never leave the SM: the kernel reads each
+// input once and writes o (and hT) once. The <true> instantiation also runs
+// the passes of the time-segmented evaluation (see TcParams).
 #include <cudaTypedefs.h>
 
 #include "kda_internal.cuh"
@@ -57,7 +59,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; then decay constants
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
-constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch | A1
+constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch
 constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
 constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major A)
 constexpr uint32_t OFF_KB = 139264;    // Kb, SW128 64 x 128 (MN-major A)
