@@ -289,6 +289,19 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
                           stream, nseg, ws, need > 0 ? sizeof(g_seg_scratch) : 0);
 }
 
+kda_status_t kda_selftest_wait_timeout(long long clocks, int* d_status, void* stream) {
+    if (clocks <= 0 || clocks > (1LL << 31))
+        return fail(KDA_ERR_INVALID_ARG, "clocks must be in 1 .. 2^31");
+    if (!d_status || ((uintptr_t)d_status & 3))
+        return fail(KDA_ERR_INVALID_ARG, "d_status must be a non-NULL, 4-byte aligned int");
+    cudaError_t e = kda::launch_selftest_wait(clocks, d_status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,
                              const float* beta, float* S, void* o, int N, int H, int dk,
                              int dv, kda_dtype_t io, int* d_status, void* stream) {

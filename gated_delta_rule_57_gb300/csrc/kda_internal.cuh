@@ -73,6 +73,7 @@ inline size_t segmented_workspace_floats(long long BH, int nseg) {
 }
 cudaError_t launch_decode(const DecodeArgs& a, kda_dtype_t io);
 cudaError_t launch_decode_multi(const MultiDecodeArgs& a, kda_dtype_t io);
+cudaError_t launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers

@@ -65,13 +65,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete, giving up after
-// ~2^31 SM clocks (about a second). Returns false on timeout; the caller
-// records the timeout and carries on without trapping.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// `limit` SM clocks (by default 2^31, about a second). Returns false on
+// timeout; the caller records the timeout and carries on without trapping.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = 1LL << 31) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > (1LL << 31)) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
 }

@@ -87,6 +87,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_chunk_fwd_segmented_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I,
                                                           I, I, I, I, I, vp, vp]
             L.kda_chunk_fwd_segmented_noalloc.restype = I
+            L.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp, vp]
+            L.kda_selftest_wait_timeout.restype = I
             L.kda_chunk_fwd_segments_hint.argtypes = [I, I, I, I, I, I]
             L.kda_chunk_fwd_segments_hint.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
@@ -223,6 +225,12 @@ def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, h0=None, *, nseg: int, o=N
                                                  nseg, _ptr(status), _stream(stream))
     _check(code)
     return o, hT
+
+
+def kda_selftest_wait_timeout(status: torch.Tensor, clocks: int = 1 << 20, stream=None):
+    """Run the bounded-wait self-test: `status` (CUDA int32, one element)
+    receives KDA_DEV_TIMEOUT when the wait gives up."""
+    _check(lib().kda_selftest_wait_timeout(clocks, _ptr(status), _stream(stream)))
 
 
 def kda_chunk_fwd_ckpt(q, k, v, g, beta, h0=None, *, ckpt_every: int, o=None, hT=None,

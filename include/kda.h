@@ -208,6 +208,18 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
 int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t io);
 
 /*
+ * Self-test of failure detection. Every wait of the kernels above on an
+ * mbarrier (TMA arrival, MMA completion) is a bounded loop: when it gives up
+ * (~2^31 SM clocks) the kernel ORs KDA_DEV_TIMEOUT into *d_status, stops, frees
+ * its tensor memory and returns, so a stuck pipeline surfaces as a status
+ * instead of a hung GPU. This launches one CTA that runs the same bounded
+ * wait on an mbarrier that nothing ever completes, giving up after `clocks`
+ * SM clocks (1 .. 2^31), and ORs KDA_DEV_TIMEOUT into *d_status (device int,
+ * required). The context stays usable afterwards.
+ */
+kda_status_t kda_selftest_wait_timeout(long long clocks, int* d_status, void* stream);
+
+/*
  * One decode step for N sequences (one token each), state updated in place
  * (section "The bill arrives in the serving stack", third bullet: the state
  * is overwritten where it lives).

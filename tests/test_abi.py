@@ -196,3 +196,10 @@ def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A
 ])
 def test_segmented_rejects(L, kw, code):
     assert call_seg(L, **kw) == code
+
+
+@pytest.mark.parametrize("clocks,status", [(0, A[0]), ((1 << 31) + 1, A[0]), (1000, None),
+                                           (1000, A[0] + 2)])
+def test_selftest_wait_rejects(L, clocks, status):
+    L.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.kda_selftest_wait_timeout(clocks, status, None) == ST.KDA_ERR_INVALID_ARG
