@@ -15,6 +15,9 @@ resident in HBM for `value`; `e2e` repeats the prefill step through the same
 C-ABI call from pinned host buffers, every input uploaded and o, hT read back
 inside the timed region, pipelined by batch row over copy and compute streams.
 
+The cpu_baseline sample doubles as a parity check ("parity"): the kernel runs
+on every batch row the oracle timed and the errors against it are reported.
+
 Prints ONE JSON line (rank 0). Under torchrun (N > 1) every rank runs its own
 independent batch on its own GPU (data-parallel sequences, no collective on
 the data path): `value` = tokens of all ranks / max over ranks of the time.
@@ -398,8 +401,9 @@ def time_prefill_long(device, seed, iters=3, warmup=1):
     return res[0], res[1], nseg, (3 if nseg > 1 else 1)
 
 
-def oracle_sample(budget_s, max_b=None):
-    """Oracle on whole batch rows of the prefill workload until ~budget_s."""
+def oracle_sample(budget_s, max_b=None, check=None):
+    """Oracle on whole batch rows of the prefill workload until ~budget_s;
+    check(x, o_ref, hT_ref), when given, sees every row (outside the timing)."""
     import oracle
     w = PREFILL
     rows = w.B if max_b is None else max_b
@@ -407,8 +411,10 @@ def oracle_sample(budget_s, max_b=None):
     for b in range(rows):
         x = inputs.prefill_inputs(w, "cpu", B=1, seed=w.seed + 101 * b)
         t0 = time.perf_counter()
-        oracle.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+        o_ref, h_ref = oracle.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
         elapsed += time.perf_counter() - t0
+        if check is not None:
+            check(x, o_ref, h_ref)
         tokens += w.T
         done += 1
         if elapsed >= budget_s:
@@ -481,13 +487,32 @@ def run_ours(args):
         }
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        tok, el, rows = oracle_sample(args.cpu_budget)
+        errs = []
+
+        def check(xr, o_ref, h_ref):
+            # the kernel on the same batch row, against the oracle's output
+            xd = {n: t.to(device) for n, t in xr.items()}
+            o, hT = kda.kda_chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["h0"])
+            torch.cuda.synchronize()
+            od = o.double().cpu().numpy()
+            eo = float(abs(od - o_ref).max() / abs(o_ref).max())
+            hd = hT.double().cpu().numpy()
+            eh = float(((hd - h_ref) ** 2).sum() ** 0.5 / (h_ref ** 2).sum() ** 0.5)
+            errs.append((eo, eh))
+
+        tok, el, rows = oracle_sample(args.cpu_budget, check=check)
         cpu = {"value": tok / el, "unit": "tokens/s", "cores": oracle.max_threads(),
                "kind": "oracle",
                "sample": f"{rows} of {w.B} batch rows x T={w.T} x H={w.H} (fp64 token loop, "
                          f"{el:.1f} s wall)"}
+        parity = {"sample": f"{rows} batch rows of the workload (T={w.T} x H={w.H} each, own "
+                            f"seeds) through kda_chunk_fwd against the fp64 oracle",
+                  "o_max_rel_err": max(e[0] for e in errs),
+                  "hT_rel_frobenius_err": max(e[1] for e in errs),
+                  "tolerance": {"o": 2e-2, "hT": 1e-2}}
 
     if rank == 0:
         line = {
@@ -506,6 +531,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "kernel": "kda_chunk_fwd (prefill)"},
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": {"value": job_value(tokens_per_rank, e2e_ms, world), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "pipelined_by_batch_row": True, "matches_device_result": e2e_exact},

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "kda_internal.cuh"
+#include <nvtx3/nvToolsExt.h>
 
 namespace {
 
@@ -15,6 +16,15 @@ void set_last_error(const char* msg) {
     strncpy(g_last_error, msg, sizeof(g_last_error) - 1);
     g_last_error[sizeof(g_last_error) - 1] = '\0';
 }
+
+// An NVTX range around each entry point (named after it), so a timeline
+// profiler shows every library call; free when no tool is attached.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -194,6 +204,7 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const fl
                            const float* beta, const float* h0, void* o, float* hT, int B,
                            int T, int H, int dk, int dv, kda_dtype_t io, void* workspace,
                            size_t ws_bytes, int* d_status, void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd");
     (void)workspace;
     (void)ws_bytes;
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0,
@@ -204,6 +215,7 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
                                 const float* beta, const float* h0, void* o, float* hT,
                                 float* ckpt, int ckpt_every, int B, int T, int H, int dk, int dv,
                                 kda_dtype_t io, int* d_status, void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd_ckpt");
     if (!ckpt) return fail(KDA_ERR_INVALID_ARG, "ckpt must be non-NULL");
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, ckpt, ckpt_every,
                           d_status, stream);
@@ -261,6 +273,7 @@ kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v
                                      float* hT, int B, int T, int H, int dk, int dv,
                                      kda_dtype_t io, int nseg, void* workspace, size_t ws_bytes,
                                      int* d_status, void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd_segmented");
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0, d_status,
                           stream, nseg, workspace, ws_bytes);
 }
@@ -270,6 +283,7 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
                                              void* o, float* hT, int B, int T, int H, int dk,
                                              int dv, kda_dtype_t io, int nseg, int* d_status,
                                              void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd_segmented_noalloc");
     const size_t need = kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, io, nseg);
     if (need == (size_t)-1)  // the full call reports which argument is wrong
         return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0,
@@ -290,6 +304,7 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
 }
 
 kda_status_t kda_selftest_wait_timeout(long long clocks, int* d_status, void* stream) {
+    NvtxRange nvtx_range("kda_selftest_wait_timeout");
     if (clocks <= 0 || clocks > (1LL << 31))
         return fail(KDA_ERR_INVALID_ARG, "clocks must be in 1 .. 2^31");
     if (!d_status || ((uintptr_t)d_status & 3))
@@ -305,6 +320,7 @@ kda_status_t kda_selftest_wait_timeout(long long clocks, int* d_status, void* st
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const float* g,
                              const float* beta, float* S, void* o, int N, int H, int dk,
                              int dv, kda_dtype_t io, int* d_status, void* stream) {
+    NvtxRange nvtx_range("kda_decode_step");
     if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
@@ -342,6 +358,7 @@ kda_status_t kda_decode_multi(const void* q, const void* k, const void* v, const
                               const float* beta, float* S, void* o, const int* ntok, int N, int K,
                               int H, int dk, int dv, kda_dtype_t io, int commit, int* d_status,
                               void* stream) {
+    NvtxRange nvtx_range("kda_decode_multi");
     if (N < 0 || H < 0 || K < 0) return fail(KDA_ERR_INVALID_ARG, "N, K and H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;

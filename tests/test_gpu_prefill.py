@@ -288,3 +288,22 @@ def test_many_heads():
     o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], h0s)
     assert_o(o[bsel][:, :, heads], o_ref, torch.bfloat16)
     assert_s(hT[bsel][:, heads], h_ref, torch.bfloat16)
+
+
+def test_chunk_size_invariance():
+    """The recurrence has no chunking: the tensor-core path (64-token chunks,
+    bf16 operands) and the CUDA-core path (32-token chunks, fp32) on the same
+    token values agree within the bf16 tolerance, and both match the oracle."""
+    w = small("bf16", 128, True)
+    x = inputs.prefill_inputs(w, DEV, B=2, T=300, H=2, seed=41)
+    o64, h64 = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    xf = {n: (t.float() if t is not None else None) for n, t in x.items()}
+    o32, h32 = kda.kda_chunk_fwd(xf["q"], xf["k"], xf["v"], xf["g"], xf["beta"], xf["h0"])
+    torch.cuda.synchronize()
+    o32n = o32.double().cpu().numpy()
+    assert_o(o64, o32n, torch.bfloat16, "C=64 vs C=32 o")
+    assert_s(h64, h32.double().cpu().numpy(), torch.bfloat16, "C=64 vs C=32 hT")
+    xc = {n: (t.cpu() if t is not None else None) for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o32, o_ref, torch.float32, "C=32 o")
+    assert_s(h32, h_ref, torch.float32, "C=32 hT")
