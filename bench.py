@@ -13,7 +13,9 @@ H=32) single-pass and split in time into parallel segments in "prefill_long"
 (--no-long skips it). Inputs are synthetic (seeded), already
 resident in HBM for `value`; `e2e` repeats the prefill step through the same
 C-ABI call from pinned host buffers, every input uploaded and o, hT read back
-inside the timed region, pipelined by batch row over copy and compute streams.
+inside the timed region, pipelined by batch row over copy and compute streams;
+its "host_link" object times the same bytes copied in and out with no compute,
+the floor the host link sets for that step.
 
 The cpu_baseline sample doubles as a parity check ("parity"): the kernel runs
 on every batch row the oracle timed and the errors against it are reported.
@@ -288,7 +290,30 @@ def time_prefill_e2e(xh, steps, warmup, device):
         step()
     end.record(s_out)
     torch.cuda.synchronize()
-    return start.elapsed_time(end) / steps, h2d, d2h, o_h, hT_h
+    e2e_ms = start.elapsed_time(end) / steps
+
+    # The host-link floor of the same step: the same bytes in and out, both
+    # directions at once, no compute. e2e / floor shows what the pipeline
+    # leaves on the table beyond the link itself.
+    def transfers():
+        s_out.wait_stream(s_in)
+        with torch.cuda.stream(s_in):
+            for n in names:
+                xd[n].copy_(xh[n], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            o_h.copy_(o_d, non_blocking=True)
+            hT_h.copy_(hT_d, non_blocking=True)
+        s_in.wait_stream(s_out)
+
+    transfers()
+    torch.cuda.synchronize()
+    start.record(s_in)
+    for _ in range(steps):
+        transfers()
+    end.record(s_in)
+    torch.cuda.synchronize()
+    floor_ms = start.elapsed_time(end) / steps
+    return e2e_ms, floor_ms, h2d, d2h, o_h, hT_h
 
 
 def time_decode(device, seed, warmup=10):
@@ -448,10 +473,11 @@ def run_ours(args):
 
     # end to end through the same call, pinned host buffers, copies timed
     xh = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "h0")}
-    e2e_ms, h2d, d2h, o_host, hT_host = time_prefill_e2e(xh, max(3, min(args.steps, 20)), 2,
-                                                          device)
+    e2e_ms, floor_ms, h2d, d2h, o_host, hT_host = time_prefill_e2e(
+        xh, max(3, min(args.steps, 20)), 2, device)
     # the pipelined host round trip must reproduce the device-resident result exactly
     e2e_exact = bool(torch.equal(o_host, o_dev.cpu()) and torch.equal(hT_host, hT_dev.cpu()))
+    floor_ms = max_over_ranks(floor_ms, world, device)
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     del xh
 
@@ -534,7 +560,11 @@ def run_ours(args):
             "parity": parity,
             "e2e": {"value": job_value(tokens_per_rank, e2e_ms, world), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "pipelined_by_batch_row": True, "matches_device_result": e2e_exact},
+                    "pipelined_by_batch_row": True, "matches_device_result": e2e_exact,
+                    "host_link": {"bound": "host link", "floor_ms_per_step": floor_ms,
+                                  "floor_gbs": (h2d + d2h) / (floor_ms * 1e-3) / 1e9,
+                                  "frac": floor_ms / e2e_ms,
+                                  "what": "the same bytes copied in and out at once, no compute"}},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "decode": {"workload": DECODE.name, "value": dec_gbs, "unit": "GB/s",
