@@ -35,7 +35,9 @@
 // chunk's g, q/k, v and beta are prefetched as soon as their buffers are free.
 // Thread 0 issues rounds 1, 3 and 4, a thread of warp 15 round 2; completion
 // is signalled through mbarriers whose waits are bounded (timeout ->
-// KDA_DEV_TIMEOUT). Intermediates never leave the SM: the kernel reads each
+// KDA_DEV_TIMEOUT). A CTA barrier stands only where a phase reads other warps'
+// results; round 1 waits on an arrive-only mbarrier instead, so the warps that
+// finish their operand rows first start their Gram-phase stores at once. Intermediates never leave the SM: the kernel reads each
 // input once and writes o (and hT) once. The <true> instantiation also runs
 // the passes of the time-segmented evaluation (see TcParams).
 #include <cudaTypedefs.h>
@@ -87,7 +89,7 @@ static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 ==
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
 
-enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, NBAR = 6 };
+enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, BAR_P1 = 6, NBAR = 7 };
 
 struct TcParams {
     const float* beta;
@@ -140,6 +142,11 @@ __device__ __forceinline__ void unpack8(uint4 u, float* x) {
         x[2 * i] = __uint_as_float(w[i] << 16);
         x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+}
+
+// CTA barrier among `count` threads (whole warps) on named barrier `id` (1..15).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // 8 consecutive bf16 (c0..c0+7, c0 % 8 == 0) of row r of an SW128 tile.
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
 
     if (tid == 0) {
-        for (int i = 0; i < NBAR; i++) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NBAR; i++) mbar_init(&bars[i], i == BAR_P1 ? kThreads : 1);
         fence_mbarrier_init();
         if (nchunks > 0) {
             prefetch_tensormap(&map_q);
@@ -485,7 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Warp = (tile a, 32-channel block cb); lane = (row pair j, 8-channel
         // group). Log-decays are kept in log2 units: each exponential is one ex2.
         bool ok = mbar_wait(&bars[BAR_QK], par) && mbar_wait(&bars[BAR_G], par);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
         {
             const int a = warp >> 2, cb = warp & 3;
             const int j = (tid & 31) >> 2, g8 = tid & 3;
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<float4*>(sgt + a * kD + c0 + 4) =
                     make_float4(tile_tot[4], tile_tot[5], tile_tot[6], tile_tot[7]);
             }
-            __syncthreads();
+            if (__syncthreads_or(!ok)) { failed = true; break; }
             // Per (tile, channel) decay constants, once, into the (now free) g buffer:
             //   0: e^{G_a-}  1: e^{G_C - G_a+}  2: e^{tile total}  3..5: e^{G_{a'-} - G_a+}, a' = 1..3
             float* CT = reinterpret_cast<float*>(sm + OFF_G);
@@ -626,11 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stash[e][2] = pack8(t8);
             }
         }
+        // Only the Gram MMA and the next g load need every warp's operands
+        // and reads done: the other warps go on to their stores at once.
         fence_proxy_async_smem();
-        __syncthreads();
+        mbar_arrive(&bars[BAR_P1]);
 
         // ------------------------------------------------------------ round 1: Gram
         if (tid == 0) {
+            if (!mbar_wait(&bars[BAR_P1], par)) flags |= KDA_DEV_TIMEOUT;
             if (c + 1 < nchunks) issue_g(c + 1);
             tc_fence_after();
             // The four windows are consecutive rows of one tile, so a single
@@ -645,7 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
-        ok = r4_wait();  // Kb, U (under [Kt; Qt]), D1 and S are free again
+        // Kb, U (under [Kt; Qt]), D1 and S are free again. (A timeout flag is
+        // only ever set by a failed wait, so it fails the vote after the readout.)
+        ok = r4_wait() && !(flags & KDA_DEV_TIMEOUT);
         if (!ok) flags |= KDA_DEV_TIMEOUT;
 #pragma unroll
         for (int e = 0; e < 2; e++) {
@@ -671,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         ok = mma_wait() && ok;
         tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        // Each warp waited for the Gram round itself; the next q, k tiles may
+        // land as soon as it is done. A failure is voted on after the readout.
         if (tid == 0 && c + 1 < nchunks) issue_qk(c + 1);
 
         // Gram readout. Quarter q: rows 32(q&1).. of A (q < 2) or P (q >= 2);
@@ -712,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
 
         // ------------------------------------------------------------ T = (I + A)^-1
         {
@@ -760,9 +772,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint32_t*>(TP + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) = 0u;
                 }
             }
-            __syncthreads();
+            // Level 2 (warps 0-3) needs only the diagonal blocks of warps 0-3,
+            // level 3 (warps 0-7) those and level 2 (its scratch slabs also
+            // overwrite rows of A that level 2 reads). The V - Y warps need
+            // neither and start as soon as round 2 is done.
+            if (warp < 4) named_sync(1, 128);
             solve_level2(FA, FT, MS, warp, tid & 31, TP, sbeta);
-            __syncthreads();
+            if (warp < 8) named_sync(2, 256);
             solve_level3(FA, FT, warp, tid & 31, TP, sbeta);
             if (warp >= 8 && q < 2) {
                 // V' = V - Y for token rows lane (0..63), value columns [64 hv, 64 hv + 64),
@@ -808,7 +824,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = mma_wait();
         tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
         if (tid == 0 && c + 1 < nchunks && !v_zero) issue_v(c + 1);
         if (q < 2) {  // U rows (scratch lanes 0..63) -> bf16 operand
             float x[32];
@@ -818,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
 
         // ------------------------------------------------------------ round 4: S += Kb^T U, O += P U
         if (tid == 0) {
