@@ -144,6 +144,23 @@ __device__ __forceinline__ void unpack8(uint4 u, float* x) {
     }
 }
 
+// Two 16-column TMEM loads (32x32b) under a single wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[16 + i]);
+    }
+}
+
 // CTA barrier among `count` threads (whole warps) on named barrier `id` (1..15).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -524,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(fabsf(sum) <= 3.402823466e38f)) flags |= KDA_DEV_NONFINITE;
             else if (mn < kLogDecayMin || mx > 0.f) flags |= KDA_DEV_DECAY_RANGE;
             // scan over the 8 row pairs of the tile (lanes g8, g8+4, ..., g8+28)
-            float tile_tot[8];
+            float tile_tot[8];  // inclusive sums: the tile totals in the last row pair (j = 7)
 #pragma unroll
             for (int z = 0; z < 8; z++) {
                 gam[1][z] += gam[0][z];
@@ -537,9 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float excl = x - gam[1][z];
                 gam[0][z] += excl;
                 gam[1][z] += excl;
-                tile_tot[z] = __shfl_sync(0xffffffffu, x, 28 + g8);
+                tile_tot[z] = x;
             }
-            if (j == 0) {
+            if (j == 7) {
                 *reinterpret_cast<float4*>(sgt + a * kD + c0) =
                     make_float4(tile_tot[0], tile_tot[1], tile_tot[2], tile_tot[3]);
                 *reinterpret_cast<float4*>(sgt + a * kD + c0 + 4) =
@@ -695,8 +712,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v0[16], v1[16];
 #pragma unroll
             for (int jj = 0; jj < 16; jj++) { v0[jj] = 0.f; v1[jj] = 0.f; }
-            if (u <= a0) tmem_ld16(tq + TM_SCR + win_row(a0) + 16 * u, v0);
-            if (u <= a0 + 1) tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * u, v1);
+            if (u <= a0)
+                tmem_ld16x2(tq + TM_SCR + win_row(a0) + 16 * u, tq + TM_SCR + win_row(a0 + 1) + 16 * u,
+                            v0, v1);
+            else if (u == a0 + 1)
+                tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * u, v1);
             const bool second = (a == a0 + 1);
             const bool live = (u <= a);
             float out[16];
