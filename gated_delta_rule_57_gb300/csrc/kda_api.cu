@@ -99,13 +99,70 @@ static __device__ __align__(256) float g_seg_scratch[12u << 20];
 
 namespace {
 
-// Segments of a split sequence: ceil(chunks / nseg) chunks each, and the
-// number of non-empty segments that gives (at most nseg).
-void segment_shape(int T, int nseg, int* seg_chunks, int* nseg_eff) {
+// Segments of a split sequence: segment 0 spans lead * sc chunks, every later
+// one sc = ceil(chunks / (lead + nseg - 1)); *nseg_eff is the number of
+// non-empty segments that gives (at most nseg).
+void segment_shape(int T, int nseg, int lead, int* seg_chunks, int* nseg_eff) {
     const int nch = (T + 63) / 64;
-    const int sc = nch > 0 ? (nch + nseg - 1) / nseg : 1;
+    const int sc = nch > 0 ? (nch + lead + nseg - 2) / (lead + nseg - 1) : 1;
     *seg_chunks = sc;
-    *nseg_eff = nch > 0 ? (nch + sc - 1) / sc : 1;
+    int ne = 1;
+    while (ne < nseg && (long long)(lead + ne - 1) * sc < nch) ne++;
+    *nseg_eff = ne;
+}
+
+// SMs of the current device, 0 if none is visible.
+int device_sms() {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        nsm <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    return nsm;
+}
+
+// Chunk steps on the critical path of a split run with one CTA per SM. The
+// segment pass starts the BH long first segments, the other SMs take the
+// 2 BH (nseg - 1) short runs (segments from zero and transitions) and every
+// SM joins once the long runs end; the correction pass has BH (nseg - 1)
+// short runs. Returns -1 when the split leaves empty segments.
+long long split_cost(long long BH, int T, int nseg, int lead, int nsm) {
+    int sc, se;
+    segment_shape(T, nseg, lead, &sc, &se);
+    if (se != nseg) return -1;
+    auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
+    const long long shorts = 2 * BH * (nseg - 1);
+    long long p1;
+    if (BH >= nsm) {
+        p1 = waves(BH) * lead * sc + waves(shorts) * sc;
+    } else {
+        const long long free_sms = nsm - BH;
+        const long long w = (shorts + free_sms - 1) / free_sms;
+        p1 = w <= lead ? (long long)lead * sc
+                       : ((long long)lead + waves(shorts - free_sms * lead)) * sc;
+    }
+    return p1 + waves(BH * (nseg - 1)) * sc;
+}
+
+// The first segment's length in short segments for a split into nseg: the
+// cheapest of 1 .. 16 that leaves as many non-empty segments as an even
+// split (so the workspace does not depend on the device); 1 without a device.
+int choose_lead(long long BH, int T, int nseg) {
+    const int nsm = device_sms();
+    if (nseg <= 1 || nsm == 0) return 1;
+    int best = 1;
+    long long best_cost = split_cost(BH, T, nseg, 1, nsm);
+    if (best_cost < 0) return 1;
+    for (int lead = 2; lead <= 16; lead++) {
+        const long long c = split_cost(BH, T, nseg, lead, nsm);
+        if (c >= 0 && c < best_cost) {
+            best_cost = c;
+            best = lead;
+        }
+    }
+    return best;
 }
 
 kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const float* g,
@@ -157,14 +214,16 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
                 return fail(KDA_ERR_INVALID_ARG, "ckpt overlaps another tensor");
     }
 
-    int seg_chunks = 0, nseg_eff = 1;
+    int seg_chunks = 0, nseg_eff = 1, lead = 1;
     if (nseg != 1) {
         if (io != KDA_BF16 || dk != 128)
             return fail(KDA_ERR_UNSUPPORTED, "segmented prefill needs bf16 and dk = dv = 128");
         const int nch = (T + 63) / 64;
         if (nseg < 1 || (T > 0 && nseg > nch))
             return fail(KDA_ERR_INVALID_ARG, "nseg must be in 1 .. ceil(T / 64)");
-        segment_shape(T, nseg, &seg_chunks, &nseg_eff);
+        segment_shape(T, nseg, 1, &seg_chunks, &nseg_eff);
+        lead = choose_lead((long long)B * H, T, nseg_eff);
+        segment_shape(T, nseg_eff, lead, &seg_chunks, &nseg_eff);
     }
     if (nseg_eff > 1) {
         const size_t need = kda::segmented_workspace_floats((long long)B * H, nseg_eff) * 4;
@@ -185,7 +244,7 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
     a.ckpt = ckpt;
     a.ckpt_every = ckpt ? ckpt_every : 0;
     cudaError_t e = nseg_eff > 1
-                        ? kda::launch_chunk_fwd_tc_segmented(a, nseg_eff, seg_chunks,
+                        ? kda::launch_chunk_fwd_tc_segmented(a, nseg_eff, seg_chunks, lead,
                                                              static_cast<float*>(workspace))
                     : io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
                                      : kda::launch_chunk_fwd_simt(a, io);
@@ -225,35 +284,50 @@ int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t
     if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return -1;
     if ((long long)B * H >= (1LL << 31)) return -1;
     if (io != KDA_BF16 || dk != 128 || B == 0 || H == 0) return 1;
-    int dev = 0, nsm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        nsm <= 0) {
-        cudaGetLastError();
-        return 1;
-    }
-    // Chunk-steps on the critical path with one sequence (or segment) per SM:
-    // whole sequences take ceil(BH / nsm) waves of nch chunks; nseg segments
-    // take the waves of the segment pass (BH * (2 nseg - 1) CTAs) and of the
-    // correction pass (BH * (nseg - 1)), each ceil(nch / nseg) chunks long.
+    const int nsm = device_sms();
+    if (nsm == 0) return 1;
+    // Chunk steps on the critical path: whole sequences take ceil(BH / nsm)
+    // waves of nch chunks; a split costs split_cost with its best first
+    // segment length plus about one chunk step per scan step. More segments
+    // mean more scan steps and workspace: take a larger count only if it
+    // saves at least 2 %.
     const long long BH = (long long)B * H, nch = (T + 63) / 64;
-    auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
-    const long long base = waves(BH) * nch;
+    const long long base = ((BH + nsm - 1) / nsm) * nch;
     int best = 1;
-    long long best_cost = base;
+    long long best_cost = -1;
     for (int s = 2; s <= 32 && s <= nch; s++) {
         int sc, se;
-        segment_shape(T, s, &sc, &se);
+        segment_shape(T, s, 1, &sc, &se);
         if (se != s) continue;
-        const long long cost = (waves(BH * (2 * s - 1)) + waves(BH * (s - 1))) * sc;
-        if (cost < best_cost) {
+        const long long c = split_cost(BH, T, s, choose_lead(BH, T, s), nsm);
+        if (c < 0) continue;
+        const long long cost = c + (s - 1);
+        if (best_cost < 0 || cost * 50 < best_cost * 49) {
             best_cost = cost;
             best = s;
         }
     }
     // Segments cost extra work (three passes over the split part) and HBM
     // traffic; take them only for a clear gain.
-    return best_cost * 5 < base * 4 ? best : 1;
+    return best_cost >= 0 && best_cost * 5 < base * 4 ? best : 1;
+}
+
+int kda_chunk_fwd_segment_plan(int B, int T, int H, int dk, int dv, kda_dtype_t io, int nseg,
+                               int* seg_chunks, int* lead) {
+    if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return -1;
+    if ((long long)B * H >= (1LL << 31)) return -1;
+    const int nch = (T + 63) / 64;
+    if (nseg < 1 || (T > 0 && nseg > nch)) return -1;
+    if (nseg > 1 && (io != KDA_BF16 || dk != 128)) return -1;
+    int sc = nch, se = 1, ld = 1;
+    if (nseg > 1) {
+        segment_shape(T, nseg, 1, &sc, &se);
+        ld = choose_lead((long long)B * H, T, se);
+        segment_shape(T, se, ld, &sc, &se);
+    }
+    if (seg_chunks) *seg_chunks = se > 1 ? sc : nch;
+    if (lead) *lead = ld;
+    return se;
 }
 
 size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int dv,
@@ -264,7 +338,7 @@ size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int d
     if (nseg < 1 || (T > 0 && nseg > nch)) return (size_t)-1;
     if (nseg > 1 && (io != KDA_BF16 || dk != 128)) return (size_t)-1;
     int sc, se;
-    segment_shape(T, nseg, &sc, &se);
+    segment_shape(T, nseg, 1, &sc, &se);
     return se > 1 ? kda::segmented_workspace_floats((long long)B * H, se) * 4 : 0;
 }
 

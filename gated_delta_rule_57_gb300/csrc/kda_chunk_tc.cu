@@ -102,13 +102,14 @@ struct TcParams {
     int ck_chunks;  // chunks between checkpoints
     int n_ckpt;
     // Segmented evaluation of long sequences (pass 0: one CTA per whole
-    // sequence). Pass 1: CTA i < BH * nseg runs segment i % nseg of sequence
-    // i / nseg from a zero state (segment 0 from h0), writing o and its final
-    // state to ws_s0; the next BH * (nseg - 1) CTAs run segments 1.. from the
-    // identity with v = 0, leaving the segment transition in ws_m. Pass 2:
-    // segments 1.. again from their incoming state ws_sin with v = 0, adding
-    // their outputs to o.
-    int pass, nseg, seg_chunks, BH;
+    // sequence). Segment 0 spans lead * seg_chunks chunks, every later one
+    // seg_chunks. Pass 1: CTA i < BH runs segment 0 of sequence i from h0
+    // (the long runs start first), the next BH * (nseg - 1) CTAs segments
+    // 1.. from a zero state, each writing o and its final state to ws_s0; the
+    // last BH * (nseg - 1) CTAs run segments 1.. from the identity with v = 0,
+    // leaving the segment transition in ws_m. Pass 2: segments 1.. again from
+    // their incoming state ws_sin with v = 0, adding their outputs to o.
+    int pass, nseg, seg_chunks, lead, BH;
     float* ws_s0;         // [BH][nseg][dk][dv]
     float* ws_m;          // [BH][nseg - 1][dk][dk]
     const float* ws_sin;  // [BH][nseg - 1][dk][dv]
@@ -356,9 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = kind == 1 ? (int)blockIdx.x - p.BH * p.nseg : (int)blockIdx.x;
             bh = j / (p.nseg - 1);
             seg = 1 + j % (p.nseg - 1);
-        } else if (SEG && p.pass == 1) {
-            bh = blockIdx.x / p.nseg;
-            seg = blockIdx.x % p.nseg;
+        } else if (SEG && p.pass == 1 && (int)blockIdx.x >= p.BH) {
+            const int j = (int)blockIdx.x - p.BH;
+            bh = j / (p.nseg - 1);
+            seg = 1 + j % (p.nseg - 1);
         }
         *bh_out = bh;
         *seg_out = seg;
@@ -366,14 +368,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bh, seg;
     task_seq(&bh, &seg);
     const int b = bh / p.H, h = bh % p.H;
-    const int t_begin = seg * p.seg_chunks * kC;
+    const int t_begin = seg == 0 ? 0 : (p.lead + seg - 1) * p.seg_chunks * kC;
     // Initial state: h0 (whole sequences and first segments), zero (other
     // segments), the identity (transition runs) or the incoming state.
     const float* h0p = kind == 2 ? p.ws_sin + ((size_t)bh * (p.nseg - 1) + seg - 1) * kD * kD
                        : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * kD * kD
                                                          : nullptr;
-    const int nchunks = (!SEG || p.pass == 0) ? (T + kC - 1) / kC
-                                              : min(p.seg_chunks, (T - t_begin + kC - 1) / kC);
+    const int nchunks = (!SEG || p.pass == 0)
+                            ? (T + kC - 1) / kC
+                            : min(seg == 0 ? p.lead * p.seg_chunks : p.seg_chunks,
+                                  (T - t_begin + kC - 1) / kC);
     const uint32_t sbase = smem_addr(sm);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* slam = reinterpret_cast<float*>(sm + OFF_LAM);
@@ -978,6 +982,7 @@ TcParams base_params(const ChunkFwdArgs& a) {
     p.pass = 0;
     p.nseg = 1;
     p.seg_chunks = 0;
+    p.lead = 1;
     p.BH = a.B * a.H;
     p.ws_s0 = p.ws_m = nullptr;
     p.ws_sin = nullptr;
@@ -1003,7 +1008,7 @@ cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
 }
 
 cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int seg_chunks,
-                                          float* ws) {
+                                          int lead, float* ws) {
     if (nseg <= 1) return launch_chunk_fwd_tc(a);
     TcMaps m;
     if (!make_maps(&m, a)) return cudaErrorInvalidValue;
@@ -1015,6 +1020,7 @@ cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int s
     TcParams p = base_params(a);
     p.nseg = nseg;
     p.seg_chunks = seg_chunks;
+    p.lead = lead;
     p.ws_s0 = s0;
     p.ws_m = mt;
     p.ws_sin = sin;

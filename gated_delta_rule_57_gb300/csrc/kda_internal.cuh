@@ -59,11 +59,12 @@ struct MultiDecodeArgs {
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_chunk_fwd_simt(const ChunkFwdArgs& a, kda_dtype_t io);
 cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a);
-// Long sequences split in time into nseg segments of seg_chunks 64-token
-// chunks (bf16, dk = dv = 128): segment pass, prefix scan, correction pass.
-// ws holds segmented_workspace_floats(B * H, nseg) floats.
+// Long sequences split in time into nseg segments (bf16, dk = dv = 128):
+// the first lead * seg_chunks 64-token chunks long, the others seg_chunks;
+// segment pass, prefix scan, correction pass. ws holds
+// segmented_workspace_floats(B * H, nseg) floats.
 cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int seg_chunks,
-                                          float* ws);
+                                          int lead, float* ws);
 cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                                 int nseg, cudaStream_t stream);
 inline size_t segmented_workspace_floats(long long BH, int nseg) {

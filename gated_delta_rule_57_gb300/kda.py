@@ -91,6 +91,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_selftest_wait_timeout.restype = I
             L.kda_chunk_fwd_segments_hint.argtypes = [I, I, I, I, I, I]
             L.kda_chunk_fwd_segments_hint.restype = I
+            L.kda_chunk_fwd_segment_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
+                                                     ctypes.POINTER(I)]
+            L.kda_chunk_fwd_segment_plan.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
             L.kda_decode_step.restype = I
             L.kda_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I,
@@ -169,6 +172,19 @@ def kda_chunk_fwd_segments_hint(B: int, T: int, H: int, dk: int, dv: int,
     if n < 0:
         raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size")
     return int(n)
+
+
+def kda_chunk_fwd_segment_plan(B: int, T: int, H: int, dk: int, dv: int,
+                               io: torch.dtype = torch.bfloat16, nseg: int = 1):
+    """The split kda_chunk_fwd_segmented uses for nseg on this device:
+    (segments, seg_chunks, lead). Segment 0 spans lead * seg_chunks 64-token
+    chunks, each later segment seg_chunks (the last may be shorter)."""
+    sc, ld = ctypes.c_int(0), ctypes.c_int(0)
+    n = lib().kda_chunk_fwd_segment_plan(B, T, H, dk, dv, _DTYPE[io], nseg, ctypes.byref(sc),
+                                         ctypes.byref(ld))
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size or nseg")
+    return int(n), int(sc.value), int(ld.value)
 
 
 def kda_chunk_fwd_segmented_workspace_size(B: int, T: int, H: int, dk: int, dv: int,

@@ -155,10 +155,13 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
  * adding their outputs to o). o and hT equal kda_chunk_fwd's up to rounding
  * (o of later segments is the sum of two bf16-rounded parts).
  *
- *   nseg      : segments per sequence, 1 .. ceil(T / 64); segments are
- *               ceil(ceil(T / 64) / nseg) chunks of 64 tokens (the last may
- *               be shorter, and fewer segments result when chunks run out);
- *               1 runs kda_chunk_fwd
+ *   nseg      : segments per sequence, 1 .. ceil(T / 64); 1 runs
+ *               kda_chunk_fwd. As many segments result as an even split into
+ *               ceil(ceil(T / 64) / nseg)-chunk segments leaves non-empty
+ *               (at most nseg); the first, which needs no transition and no
+ *               correction, may span several segment lengths so that its long
+ *               runs overlap the other segments' passes on the remaining SMs
+ *               (kda_chunk_fwd_segment_plan gives the split for the device)
  *   workspace : device buffer of kda_chunk_fwd_segmented_workspace_size bytes,
  *               16-byte aligned, not overlapping any other tensor; contents
  *               are scratch
@@ -206,6 +209,20 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
  * has no segmented path. -1 for arguments kda_chunk_fwd would reject.
  */
 int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t io);
+
+/*
+ * The split kda_chunk_fwd_segmented uses for nseg on the current device:
+ * returns the number of segments that results (1 = no split), or -1 for
+ * arguments kda_chunk_fwd_segmented would reject. *seg_chunks (if not NULL)
+ * receives the length of every segment after the first in 64-token chunks
+ * (the last may be shorter; ceil(T / 64) when there is no split) and *lead
+ * (if not NULL) the first segment's length in those units. The first segment
+ * length is the one of 1 .. 16 that minimises the chunk steps on the critical
+ * path when the segment pass starts the first segments' long runs on B * H
+ * SMs and the other runs on the rest; 1 when no CUDA device is visible.
+ */
+int kda_chunk_fwd_segment_plan(int B, int T, int H, int dk, int dv, kda_dtype_t io, int nseg,
+                               int* seg_chunks, int* lead);
 
 /*
  * Self-test of failure detection. Every wait of the kernels above on an

@@ -177,6 +177,35 @@ def test_segments_hint(L):
     assert L.kda_chunk_fwd_segments_hint(-1, 4096, 32, 128, 128, kda.KDA_BF16) == -1
 
 
+def test_segment_plan(L):
+    f = L.kda_chunk_fwd_segment_plan
+    f.restype = ctypes.c_int
+    sc, lead = ctypes.c_int(0), ctypes.c_int(0)
+
+    def plan(B, T, H, nseg, dk=128, io=kda.KDA_BF16):
+        return f(B, T, H, dk, dk, io, nseg, ctypes.byref(sc), ctypes.byref(lead))
+
+    # covers the chunks with the workspace's segment count, whatever the lead
+    for B, T, H, nseg in ((1, 1 << 20, 32, 10), (1, 1000, 2, 7), (1, 2048, 32, 8), (2, 640, 3, 10)):
+        n = plan(B, T, H, nseg)
+        nch = (T + 63) // 64
+        even = -(-nch // nseg)
+        assert n == -(-nch // even)  # non-empty segments of the even split
+        assert lead.value >= 1 and (lead.value + n - 1) * sc.value >= nch
+        assert (lead.value + n - 2) * sc.value < nch  # the last segment is not empty
+        ws = L.kda_chunk_fwd_segmented_workspace_size
+        ws.restype = ctypes.c_size_t
+        assert ws(B, T, H, 128, 128, kda.KDA_BF16, nseg) == B * H * (3 * n - 2) * 128 * 128 * 4
+    assert plan(1, 4096, 32, 1) == 1 and sc.value == 64 and lead.value == 1
+    assert plan(1, 0, 32, 3) == 1
+    assert plan(1, 4096, 32, 0) == -1
+    assert plan(1, 4096, 32, 65) == -1  # more segments than chunks
+    assert plan(1, 4096, 32, 2, io=kda.KDA_F32) == -1
+    assert plan(1, 4096, 32, 2, dk=64) == -1
+    assert plan(-1, 4096, 32, 2) == -1
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 4, None, None) == 4  # outputs optional
+
+
 def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A[0]):
     # T = 128: two chunks; every tensor fits the 64 KB spacing of the fake addresses
     return L.kda_chunk_fwd_segmented(q, A[1], A[2], A[3], A[4], None, A[5], A[6], 1, T, 1, dk,

@@ -27,17 +27,34 @@ def run_seg(x, nseg, **kw):
 
 
 @pytest.mark.parametrize("B,T,H,nseg,h0", [
-    (1, 1000, 2, 3, True),     # 16 chunks: segments of 6, 6, 4 (ragged last chunk)
+    (1, 1000, 2, 3, True),     # 16 chunks in 3 segments (ragged last chunk)
     (2, 640, 3, 10, False),    # one chunk per segment
     (1, 129, 1, 2, True),      # 3 chunks: 2 + 1, last segment a single ragged token
     (3, 2048, 2, 4, True),
-    (1, 1000, 2, 7, True),     # 16 chunks, nseg 7 -> segments of 3 (6 of them)
+    (1, 1000, 2, 7, True),     # 16 chunks, nseg 7 -> 6 non-empty segments
 ])
 def test_segmented_matches_oracle(B, T, H, nseg, h0):
     x = inputs.prefill_inputs(workload(h0), DEV, B=B, T=T, H=H, seed=B * 1000 + T + nseg)
     o, hT, st = run_seg(x, nseg)
     assert st == 0
     xc = {n: (t.cpu() if t is not None else None) for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, BF16)
+    assert_s(hT, h_ref, BF16)
+
+
+def test_long_first_segment_matches_oracle():
+    """B=1, H=32, T=2048, nseg=8: the 224 short runs of the segment pass
+    exceed the 120 SMs the first segments leave free, so the first segment
+    spans several segment lengths (on 152 SMs: 12 chunks, then 3-chunk
+    segments and a 2-chunk last one)."""
+    n, sc, lead = kda.kda_chunk_fwd_segment_plan(1, 2048, 32, 128, 128, nseg=8)
+    assert n == 8 and lead > 1, (n, sc, lead)
+    assert (lead + n - 1) * sc >= 32 > (lead + n - 2) * sc
+    x = inputs.prefill_inputs(workload(True), DEV, B=1, T=2048, H=32, seed=15)
+    o, hT, st = run_seg(x, 8)
+    assert st == 0
+    xc = {nm: (t.cpu() if t is not None else None) for nm, t in x.items()}
     o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
     assert_o(o, o_ref, BF16)
     assert_s(hT, h_ref, BF16)
