@@ -43,15 +43,16 @@ def test_segmented_matches_oracle(B, T, H, nseg, h0):
     assert_s(hT, h_ref, BF16)
 
 
-def test_long_first_segment_matches_oracle():
-    """B=1, H=32, T=2048, nseg=8: the 224 short runs of the segment pass
+@pytest.mark.parametrize("T", [2048, 2000])
+def test_long_first_segment_matches_oracle(T):
+    """B=1, H=32, 32 chunks, nseg=8: the 224 short runs of the segment pass
     exceed the 120 SMs the first segments leave free, so the first segment
     spans several segment lengths (on 152 SMs: 12 chunks, then 3-chunk
-    segments and a 2-chunk last one)."""
-    n, sc, lead = kda.kda_chunk_fwd_segment_plan(1, 2048, 32, 128, 128, nseg=8)
+    segments and a 2-chunk last one, ragged at T = 2000)."""
+    n, sc, lead = kda.kda_chunk_fwd_segment_plan(1, T, 32, 128, 128, nseg=8)
     assert n == 8 and lead > 1, (n, sc, lead)
     assert (lead + n - 1) * sc >= 32 > (lead + n - 2) * sc
-    x = inputs.prefill_inputs(workload(True), DEV, B=1, T=2048, H=32, seed=15)
+    x = inputs.prefill_inputs(workload(True), DEV, B=1, T=T, H=32, seed=15)
     o, hT, st = run_seg(x, 8)
     assert st == 0
     xc = {nm: (t.cpu() if t is not None else None) for nm, t in x.items()}
