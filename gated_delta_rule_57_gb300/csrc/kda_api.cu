@@ -146,12 +146,12 @@ long long split_cost(long long BH, int T, int nseg, int lead, int nsm) {
     return p1 + waves(BH * (nseg - 1)) * sc;
 }
 
-// The first segment's length in short segments for a split into nseg: the
-// cheapest of 1 .. 16 that leaves as many non-empty segments as an even
-// split (so the workspace does not depend on the device); 1 without a device.
-int choose_lead(long long BH, int T, int nseg) {
-    const int nsm = device_sms();
-    if (nseg <= 1 || nsm == 0) return 1;
+// The first segment's length in short segments for a split into nseg on nsm
+// SMs: the cheapest of 1 .. 16 that leaves as many non-empty segments as an
+// even split (so the workspace does not depend on the device); 1 without a
+// device (nsm = 0).
+int choose_lead(long long BH, int T, int nseg, int nsm) {
+    if (nseg <= 1 || nsm <= 0) return 1;
     int best = 1;
     long long best_cost = split_cost(BH, T, nseg, 1, nsm);
     if (best_cost < 0) return 1;
@@ -222,7 +222,7 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
         if (nseg < 1 || (T > 0 && nseg > nch))
             return fail(KDA_ERR_INVALID_ARG, "nseg must be in 1 .. ceil(T / 64)");
         segment_shape(T, nseg, 1, &seg_chunks, &nseg_eff);
-        lead = choose_lead((long long)B * H, T, nseg_eff);
+        lead = choose_lead((long long)B * H, T, nseg_eff, device_sms());
         segment_shape(T, nseg_eff, lead, &seg_chunks, &nseg_eff);
     }
     if (nseg_eff > 1) {
@@ -299,7 +299,7 @@ int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t
         int sc, se;
         segment_shape(T, s, 1, &sc, &se);
         if (se != s) continue;
-        const long long c = split_cost(BH, T, s, choose_lead(BH, T, s), nsm);
+        const long long c = split_cost(BH, T, s, choose_lead(BH, T, s, nsm), nsm);
         if (c < 0) continue;
         const long long cost = c + (s - 1);
         if (best_cost < 0 || cost * 50 < best_cost * 49) {
@@ -322,7 +322,7 @@ int kda_chunk_fwd_segment_plan(int B, int T, int H, int dk, int dv, kda_dtype_t 
     int sc = nch, se = 1, ld = 1;
     if (nseg > 1) {
         segment_shape(T, nseg, 1, &sc, &se);
-        ld = choose_lead((long long)B * H, T, se);
+        ld = choose_lead((long long)B * H, T, se, device_sms());
         segment_shape(T, se, ld, &sc, &se);
     }
     if (seg_chunks) *seg_chunks = se > 1 ? sc : nch;
