@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include <nvtx3/nvToolsExt.h>
 
@@ -92,10 +94,38 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
 }  // extern "C"
 
 // Scratch of kda_chunk_fwd_segmented_noalloc: 48 MB in the library's own
-// device image (one instance per device, set up when the module loads), so
-// that entry point allocates nothing. It holds the (3 nseg - 2) 64 KB states
-// per sequence of e.g. 32 sequences x 8 segments.
+// device image, so that entry point allocates nothing. Every device that loads
+// the library holds one instance until the process exits. It holds the
+// (3 nseg - 2) 64 KB states per sequence of e.g. 48 sequences x 6 segments or
+// 32 sequences x 8 segments.
 static __device__ __align__(256) float g_seg_scratch[12u << 20];
+
+namespace {
+
+// Device address of g_seg_scratch, taken once per device (with that device
+// current) on the first no-allocation call there. In host code the array's
+// name is only a host-side stand-in, so kernels get this address instead.
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t seg_scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_seg_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
 
 namespace {
 
@@ -169,7 +199,8 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
                             const float* beta, const float* h0, void* o, float* hT, int B,
                             int T, int H, int dk, int dv, kda_dtype_t io, float* ckpt,
                             int ckpt_every, int* d_status, void* stream, int nseg = 1,
-                            void* workspace = nullptr, size_t ws_bytes = 0) {
+                            void* workspace = nullptr, size_t ws_bytes = 0,
+                            bool check_only = false) {
     if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
@@ -225,6 +256,8 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
         lead = choose_lead((long long)B * H, T, nseg_eff, device_sms());
         segment_shape(T, nseg_eff, lead, &seg_chunks, &nseg_eff);
     }
+    // Every argument but the workspace is valid.
+    if (check_only) return KDA_OK;
     if (nseg_eff > 1) {
         const size_t need = kda::segmented_workspace_floats((long long)B * H, nseg_eff) * 4;
         if (!workspace || ws_bytes < need)
@@ -358,16 +391,16 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
                                              int dv, kda_dtype_t io, int nseg, int* d_status,
                                              void* stream) {
     NvtxRange nvtx_range("kda_chunk_fwd_segmented_noalloc");
+    // Argument errors first, as for the other entry points.
+    kda_status_t st = chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr,
+                                     0, d_status, stream, nseg, nullptr, 0, /*check_only=*/true);
+    if (st != KDA_OK) return st;
     const size_t need = kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, io, nseg);
-    if (need == (size_t)-1)  // the full call reports which argument is wrong
-        return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0,
-                              d_status, stream, nseg, nullptr, 0);
     if (need > sizeof(g_seg_scratch))
-        return fail(KDA_ERR_WORKSPACE, "problem needs more than the static segment scratch");
+        return fail(KDA_ERR_WORKSPACE, "problem needs more than the 48 MB static segment scratch");
     void* ws = nullptr;
     if (need > 0) {
-        // the array has one instance per device: take the current device's
-        cudaError_t e = cudaGetSymbolAddress(&ws, g_seg_scratch);
+        cudaError_t e = seg_scratch_address(&ws);
         if (e != cudaSuccess) {
             set_last_error(cudaGetErrorString(e));
             return KDA_ERR_CUDA;

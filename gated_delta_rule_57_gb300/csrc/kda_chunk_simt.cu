@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(NT, 1)
             float acc = 0.f;
             for (int i = 0; i < DK; i++) acc += sm.Q[r * LDK + i] * sm.S[i * LDV + j];
             for (int s = 0; s <= r; s++) acc += sm.P[r * LDC + s] * sm.V[s * LDV + j];
+            flags |= finite_flag(acc);  // a NaN or Inf in q, k or v reaches some output
             o[(((size_t)b * T + t0 + r) * H + h) * DV + j0 + j] = from_f32<TIn>(acc);
         }
         __syncthreads();

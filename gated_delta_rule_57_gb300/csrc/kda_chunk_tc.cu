@@ -466,6 +466,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kind == 1) return;
         float x[32];
         tmem_ld32(tq + TM_D1 + 32 * u, x);
+        // A NaN or Inf in q, k or v reaches some output through the
+        // recurrence; x * 0 is 0 for finite x and NaN otherwise.
+        float probe = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; e++) probe = fmaf(x[e], 0.f, probe);
+        if (probe != 0.f) flags |= KDA_DEV_NONFINITE;
         if (lane - 64 < len) {
             __nv_bfloat16* dst =
                 p.o + (((size_t)b * T + t_begin + cc * kC + lane - 64) * p.H + h) * kD + 32 * u;

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         float kv = to_f32(k[head * DK + i]);
         float qv = to_f32(q[head * DK + i]);
         float gv = g[head * DK + i];
-        flags |= decay_flags(gv);
+        flags |= decay_flags(gv) | finite_flag(kv) | finite_flag(qv);
         s_k[i] = kv;
         s_q[i] = qv;
         s_a[i] = expf(gv);
@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(NT, 512 / NT)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
     if ((tid & 31) == 0) s_kq[tid >> 5] = kq;
-    report_flags(d_status, flags);
     __syncthreads();
 
     // S' = Diag(exp g) S, and partial sums of S'^T k and S'^T q.
@@ -113,7 +112,9 @@ __global__ void __launch_bounds__(NT, 512 / NT)
             kvj += s_red[0][w][j];
             qvj += s_red[1][w][j];
         }
-        u[c] = b * (to_f32(v[head * DV + j0 + j]) - kvj);
+        const float vj = to_f32(v[head * DV + j0 + j]);
+        flags |= finite_flag(vj);
+        u[c] = b * (vj - kvj);
         if (rg == 0) o[head * DV + j0 + j] = from_f32<TIn>(qvj + u[c] * kqt);
     }
 
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         st[r].w += ki * u[3];
         Sh[(size_t)(rg + r * RG) * (DV / 4) + cg] = st[r];
     }
+    report_flags(d_status, flags);
 }
 
 template <typename TIn, int D>

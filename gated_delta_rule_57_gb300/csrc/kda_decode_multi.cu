@@ -11,172 +11,178 @@
 //                        each sequence, written back in place (o optional).
 // Per token it is the decode recurrence
 //     S' = Diag(exp g) S,  u = beta (v - S'^T k),  S = S' + k u^T,
-//     o  = S^T q = S'^T q + u (k . q).
-// The state slice stays in registers for all K tokens: it is read once and
-// written at most once, so K tokens cost about the HBM traffic of one
-// single-token step.
+//     o  = S^T q = S'^T q + u (k . q),
+// evaluated with S'^T k = S^T (e^g k) and S'^T q = S^T (e^g q), so both
+// reductions read the state before its decay.
+//
+// Layout. One warp per (sequence, head, 32-column slice of the value
+// channels); the D / 32 warps of a head form one CTA and share its staged
+// token vectors. Lane l owns columns j0 + 4 (l % 8) .. + 3 of rows
+// (l / 8) * D/4 .. + D/4 - 1 in registers (32 float4 at D = 128) for all the
+// sequence's tokens: the state is read once and written at most once. The
+// reductions over the key channel finish inside the warp (two xor-shuffle
+// steps across the four row groups), so the token loop has no barrier; the
+// token vectors (e^g k, e^g q, k, e^g, v, beta, k . q) are staged in shared
+// memory eight tokens at a time, with one barrier per eight tokens.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-// One CTA per (sequence, head, DVS-wide slice of the value columns): the
-// columns of S evolve independently given k, g, beta, so a slice only needs
-// its own v columns. Small CTAs let several per SM overlap one CTA's per-token
-// reductions with another's state streaming.
-template <typename TIn, int DK, int DVS, int NT>
-__global__ void __launch_bounds__(NT, 512 / NT)
+constexpr int kStage = 8;  // tokens staged per pass
+
+template <typename TIn, int D>
+__global__ void __launch_bounds__(D, 384 / D)
     kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                             const TIn* __restrict__ v, const float* __restrict__ g,
                             const float* __restrict__ beta, float* __restrict__ S,
                             TIn* __restrict__ o, const int* __restrict__ ntok, int K, int H,
-                            int DV, int commit, int* __restrict__ d_status) {
-    constexpr int CG = DVS / 4;   // float4 column groups per state row slice
-    constexpr int RG = NT / CG;   // row groups
-    constexpr int RPT = DK / RG;  // rows per thread
-    constexpr int NW = NT / 32;
-    static_assert(NT % CG == 0 && DK % RG == 0, "bad tiling");
+                            int commit, int* __restrict__ d_status) {
+    constexpr int R = D / 4;    // state rows per thread
+    constexpr int NW = D / 32;  // warps = 32-column value slices per head
+    // Key-channel vectors keep four padding words after each row group's R
+    // entries, so the four row groups' float4 reads fall on distinct banks.
+    constexpr int LDP = D + 16;
+    __shared__ __align__(16) float s_lk[kStage][LDP], s_lq[kStage][LDP], s_k[kStage][LDP],
+        s_lam[kStage][LDP];
+    __shared__ __align__(16) float s_v[kStage][D];
+    __shared__ float s_kqp[kStage][NW], s_beta[kStage];
 
-    // Token vectors and reduction buffers are double-buffered by token parity,
-    // so a token costs three barriers.
-    __shared__ float s_k[2][DK], s_q[2][DK], s_a[2][DK];
-    __shared__ float s_red[2][2][RG][DVS];
-    __shared__ __align__(16) float s_tot[2][2][DVS];  // column totals of S'^T k and S'^T q
-    static_assert(NT == 2 * DVS, "one thread per (column, reduction)");
-    __shared__ float s_kq[2][NW];
-
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t head = blockIdx.x;  // n * H + h
     const int n = (int)(head / H), hh = (int)(head % H);
-    const int j0 = blockIdx.y * DVS;  // first value column of this slice
-    const int cg = tid % CG, rg = tid / CG;
-    const int RS = DV / 4;  // float4 per full state row
+    const int cg = lane & 7, rg = lane >> 3;
+    const int j = 32 * warp + 4 * cg;  // first of this thread's four value columns
+    const int i0 = rg * R;             // first of its state rows
+    const int p0 = rg * (R + 4);       // where they start in the padded vectors
+    const int ptid = tid + (tid / R) * 4;
     int nt = K;
     if (ntok) nt = min(max(ntok[n], 0), K);
-    float4* Sh = reinterpret_cast<float4*>(S + head * DK * DV + j0);
+    if (nt == 0) return;
+    float4* Sh = reinterpret_cast<float4*>(S + head * D * D + j);
 
-    float4 st[RPT];
+    float4 st[R];
 #pragma unroll
-    for (int r = 0; r < RPT; r++) st[r] = Sh[(size_t)(rg + r * RG) * RS + cg];
-
-    // The next token's inputs are loaded into registers while the current one
-    // is processed, so their HBM latency is off the per-token chain.
-    constexpr int PER = (DK + NT - 1) / NT;  // key channels per thread (<= 1 here)
-    float nk[PER], nq[PER], ng[PER], nv[4], nb = 0.f;
-    auto fetch = [&](int t) {
-        const size_t row = ((size_t)n * K + t) * H + hh;
-#pragma unroll
-        for (int p = 0; p < PER; p++) {
-            const int i = tid + p * NT;
-            if (i < DK) {
-                nk[p] = to_f32(k[row * DK + i]);
-                nq[p] = to_f32(q[row * DK + i]);
-                ng[p] = g[row * DK + i];
-            }
-        }
-#pragma unroll
-        for (int c = 0; c < 4; c++) nv[c] = to_f32(v[row * DV + j0 + cg * 4 + c]);
-        nb = beta[row];
-    };
-    if (nt > 0) fetch(0);
+    for (int r = 0; r < R; r++) st[r] = Sh[(size_t)(i0 + r) * (D / 4)];
 
     int flags = 0;
-    for (int t = 0; t < nt; t++) {
-        const int buf = t & 1;
-        const size_t row = ((size_t)n * K + t) * H + hh;
-        float kq = 0.f;
+    for (int t0 = 0; t0 < nt; t0 += kStage) {
+        const int nb = min(kStage, nt - t0);
+        if (t0 > 0) __syncthreads();  // the previous block's vectors are consumed
+        // Stage: thread tid owns key channel (and value column) tid of each token.
+        for (int tt = 0; tt < nb; tt++) {
+            const size_t row = ((size_t)n * K + t0 + tt) * H + hh;
+            const float kv = to_f32(k[row * D + tid]);
+            const float qv = to_f32(q[row * D + tid]);
+            const float gv = g[row * D + tid];
+            const float vv = to_f32(v[row * D + tid]);
+            flags |= decay_flags(gv) | finite_flag(kv) | finite_flag(qv) | finite_flag(vv);
+            const float lam = expf(gv);
+            s_k[tt][ptid] = kv;
+            s_lam[tt][ptid] = lam;
+            s_lk[tt][ptid] = lam * kv;
+            s_lq[tt][ptid] = lam * qv;
+            s_v[tt][tid] = vv;
+            float kq = kv * qv;
 #pragma unroll
-        for (int p = 0; p < PER; p++) {
-            const int i = tid + p * NT;
-            if (i < DK) {
-                flags |= decay_flags(ng[p]);
-                s_k[buf][i] = nk[p];
-                s_q[buf][i] = nq[p];
-                s_a[buf][i] = expf(ng[p]);
-                kq += nk[p] * nq[p];
+            for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            if (lane == 0) s_kqp[tt][warp] = kq;
+        }
+        if (tid < nb) {
+            const float b = beta[((size_t)n * K + t0 + tid) * H + hh];
+            flags |= finite_flag(b);
+            s_beta[tid] = b;
+        }
+        __syncthreads();
+
+        for (int tt = 0; tt < nb; tt++) {
+            // a = S^T (e^g k), b = S^T (e^g q) over this thread's rows
+            float a[4] = {0.f, 0.f, 0.f, 0.f}, bq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r4 = 0; r4 < R; r4 += 4) {
+                const float4 lk = *reinterpret_cast<const float4*>(&s_lk[tt][p0 + r4]);
+                const float4 lq = *reinterpret_cast<const float4*>(&s_lq[tt][p0 + r4]);
+                const float lkv[4] = {lk.x, lk.y, lk.z, lk.w};
+                const float lqv[4] = {lq.x, lq.y, lq.z, lq.w};
+#pragma unroll
+                for (int rr = 0; rr < 4; rr++) {
+                    const float4 s4 = st[r4 + rr];
+                    a[0] = fmaf(s4.x, lkv[rr], a[0]);
+                    a[1] = fmaf(s4.y, lkv[rr], a[1]);
+                    a[2] = fmaf(s4.z, lkv[rr], a[2]);
+                    a[3] = fmaf(s4.w, lkv[rr], a[3]);
+                    bq[0] = fmaf(s4.x, lqv[rr], bq[0]);
+                    bq[1] = fmaf(s4.y, lqv[rr], bq[1]);
+                    bq[2] = fmaf(s4.z, lqv[rr], bq[2]);
+                    bq[3] = fmaf(s4.w, lqv[rr], bq[3]);
+                }
+            }
+            // totals over the four row groups (lanes l, l ^ 8, l ^ 16, l ^ 24)
+#pragma unroll
+            for (int off = 8; off < 32; off <<= 1) {
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    a[c] += __shfl_xor_sync(0xffffffffu, a[c], off);
+                    bq[c] += __shfl_xor_sync(0xffffffffu, bq[c], off);
+                }
+            }
+            float kq = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; w++) kq += s_kqp[tt][w];
+            const float bt = s_beta[tt];
+            const float4 v4 = *reinterpret_cast<const float4*>(&s_v[tt][j]);
+            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float u[4], ov[4];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                u[c] = bt * (vv[c] - a[c]);
+                ov[c] = bq[c] + u[c] * kq;
+            }
+            if (o && rg == (tt & 3)) {  // the four row groups take turns storing
+                TIn* dst = o + (((size_t)n * K + t0 + tt) * H + hh) * D + j;
+                if constexpr (sizeof(TIn) == 2) {
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(ov[0], ov[1]);
+                    __nv_bfloat162 h1 = __floats2bfloat162_rn(ov[2], ov[3]);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<uint32_t*>(&h0);
+                    pk.y = *reinterpret_cast<uint32_t*>(&h1);
+                    *reinterpret_cast<uint2*>(dst) = pk;
+                } else {
+                    *reinterpret_cast<float4*>(dst) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+                }
+            }
+            // S = Diag(e^g) S + k u^T
+#pragma unroll
+            for (int r4 = 0; r4 < R; r4 += 4) {
+                const float4 kk = *reinterpret_cast<const float4*>(&s_k[tt][p0 + r4]);
+                const float4 ll = *reinterpret_cast<const float4*>(&s_lam[tt][p0 + r4]);
+                const float kv[4] = {kk.x, kk.y, kk.z, kk.w};
+                const float lv[4] = {ll.x, ll.y, ll.z, ll.w};
+#pragma unroll
+                for (int rr = 0; rr < 4; rr++) {
+                    float4& s4 = st[r4 + rr];
+                    s4.x = fmaf(lv[rr], s4.x, kv[rr] * u[0]);
+                    s4.y = fmaf(lv[rr], s4.y, kv[rr] * u[1]);
+                    s4.z = fmaf(lv[rr], s4.z, kv[rr] * u[2]);
+                    s4.w = fmaf(lv[rr], s4.w, kv[rr] * u[3]);
+                }
             }
         }
-        const float b = nb;
-        float vj[4];
-#pragma unroll
-        for (int c = 0; c < 4; c++) vj[c] = nv[c];
-        if (tid == 0) flags |= finite_flag(b);
-        if (t + 1 < nt) fetch(t + 1);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-        if ((tid & 31) == 0) s_kq[buf][tid >> 5] = kq;
-        __syncthreads();
-
-        float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < RPT; r++) {
-            const int i = rg + r * RG;
-            const float a = s_a[buf][i], ki = s_k[buf][i], qi = s_q[buf][i];
-            st[r].x *= a;
-            st[r].y *= a;
-            st[r].z *= a;
-            st[r].w *= a;
-            pk[0] += st[r].x * ki;
-            pk[1] += st[r].y * ki;
-            pk[2] += st[r].z * ki;
-            pk[3] += st[r].w * ki;
-            pq[0] += st[r].x * qi;
-            pq[1] += st[r].y * qi;
-            pq[2] += st[r].z * qi;
-            pq[3] += st[r].w * qi;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-            s_red[buf][0][rg][cg * 4 + c] = pk[c];
-            s_red[buf][1][rg][cg * 4 + c] = pq[c];
-        }
-        __syncthreads();
-
-        {  // thread tid sums one column total over the RG row groups
-            const int which = tid / DVS, col = tid % DVS;
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < RG; w++) acc += s_red[buf][which][w][col];
-            s_tot[buf][which][col] = acc;
-        }
-        __syncthreads();
-        float kqt = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; w++) kqt += s_kq[buf][w];
-        float u[4];
-        const float4 kv4 = *reinterpret_cast<const float4*>(&s_tot[buf][0][cg * 4]);
-        const float4 qv4 = *reinterpret_cast<const float4*>(&s_tot[buf][1][cg * 4]);
-        const float kvs[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
-        const float qvs[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-            u[c] = b * (vj[c] - kvs[c]);
-            if (o && rg == 0) o[row * DV + j0 + cg * 4 + c] = from_f32<TIn>(qvs[c] + u[c] * kqt);
-        }
-#pragma unroll
-        for (int r = 0; r < RPT; r++) {
-            const float ki = s_k[buf][rg + r * RG];
-            st[r].x += ki * u[0];
-            st[r].y += ki * u[1];
-            st[r].z += ki * u[2];
-            st[r].w += ki * u[3];
-        }
     }
-    if (commit && nt > 0) {
+    if (commit) {
 #pragma unroll
-        for (int r = 0; r < RPT; r++) Sh[(size_t)(rg + r * RG) * RS + cg] = st[r];
+        for (int r = 0; r < R; r++) Sh[(size_t)(i0 + r) * (D / 4)] = st[r];
     }
     report_flags(d_status, flags);
 }
 
 template <typename TIn, int D>
 cudaError_t launch_t(const MultiDecodeArgs& a) {
-    constexpr int DVS = 32, NT = 64;
-    const dim3 grid((unsigned)((long long)a.N * a.H), D / DVS);
-    kda_decode_multi_kernel<TIn, D, DVS, NT><<<grid, NT, 0, a.stream>>>(
+    const unsigned grid = (unsigned)((long long)a.N * a.H);
+    kda_decode_multi_kernel<TIn, D><<<grid, D, 0, a.stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
         static_cast<const TIn*>(a.v), a.g, a.beta, a.S, static_cast<TIn*>(a.o), a.ntok, a.K,
-        a.H, D, a.commit, a.d_status);
+        a.H, a.commit, a.d_status);
     return cudaGetLastError();
 }
 

@@ -62,7 +62,7 @@ typedef enum {
     KDA_ERR_WORKSPACE = 3,   /* workspace pointer or size too small */
     KDA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
     KDA_ERR_DECAY_RANGE = 5, /* (device) some g outside [-5, 0] */
-    KDA_ERR_NONFINITE = 6,   /* (device) NaN or Inf in g or beta */
+    KDA_ERR_NONFINITE = 6,   /* (device) NaN or Inf in an input */
     KDA_ERR_TIMEOUT = 7      /* (device) a bounded on-chip wait gave up */
 } kda_status_t;
 
@@ -70,7 +70,13 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
 
 /* Bits OR-ed into *d_status by the kernels. */
 #define KDA_DEV_DECAY_RANGE 0x1 /* some g < -5 or g > 0 */
-#define KDA_DEV_NONFINITE 0x2   /* some g or beta is NaN or Inf */
+/* Some q, k, v, g or beta is NaN or Inf. g and beta are checked as they are
+ * read; the decode kernels also check q, k and v as they are read. The
+ * prefill kernels find a NaN or Inf in q, k or v through the outputs: any
+ * of them makes some o non-finite through the recurrence, so they check
+ * every o they compute (which also catches a non-finite h0 or an o that
+ * overflows fp32). */
+#define KDA_DEV_NONFINITE 0x2
 #define KDA_DEV_TIMEOUT 0x4     /* an mbarrier wait exceeded its iteration cap */
 
 /* Version of this header the library was built from (KDA_ABI_VERSION). */
@@ -187,13 +193,32 @@ size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int d
                                               kda_dtype_t io, int nseg);
 
 /*
- * kda_chunk_fwd_segmented with the scratch in a fixed 48 MB device array of
- * the library (one per device; its address is taken on the current device at
- * each call), so the call allocates nothing and takes no workspace argument.
- * Problems whose kda_chunk_fwd_segmented_workspace_size exceeds 48 MB return
- * KDA_ERR_WORKSPACE before any launch. The array is shared by every call on
- * a device: calls must not run concurrently on different streams of the
- * same device. Other arguments and errors as for kda_chunk_fwd_segmented.
+ * kda_chunk_fwd_segmented for callers that cannot allocate device memory: the
+ * call takes no workspace and allocates nothing. Such callers include
+ * serving runtimes that reserve all device memory up front and hand the
+ * library none of it, and memory-pool or allocator plugins that must not call
+ * back into the allocator that is running them. The paper has no
+ * counterpart: this is a deployment variant of kda_chunk_fwd_segmented.
+ *
+ * The scratch is a 48 MB array in the library's own device image; every GPU
+ * that loads the library holds one copy until the process exits. Its device
+ * address is looked up once per device, by the first call of this function on
+ * that device (with the device current); make that first call before any
+ * stream capture. Limits and sharing:
+ *   - kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, io, nseg) must
+ *     be at most 48 MB, i.e. B * H * (3 nseg' - 2) <= 768 with nseg' the
+ *     number of segments that results (e.g. nseg <= 8 at B = 1, H = 32;
+ *     nseg <= 6 at B * H = 48). The count kda_chunk_fwd_segments_hint
+ *     returns can exceed this (it does at B = 1, T = 2^20, H = 32): pass a
+ *     smaller nseg here. A larger problem returns KDA_ERR_WORKSPACE before
+ *     any launch.
+ *   - Every call on a device shares the array: calls whose work overlaps on
+ *     the GPU (different streams, or host threads) race and give wrong
+ *     results; serialise them on one stream. The array keeps the last call's
+ *     contents; nothing in it needs to start at zero (every value is written
+ *     before it is read).
+ * Argument errors are checked first, as for kda_chunk_fwd_segmented; other
+ * arguments, results and errors are those of kda_chunk_fwd_segmented.
  */
 kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
                                              const float* g, const float* beta, const float* h0,

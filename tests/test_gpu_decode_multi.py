@@ -90,3 +90,16 @@ def test_multi_status_flags():
     kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & kda.KDA_DEV_DECAY_RANGE
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v"])
+def test_multi_nonfinite_qkv_is_flagged(name):
+    x = draft(2, 3, 2, 128, "bf16", 26)
+    x[name][1, 2, 1, 40] = float("nan")
+    for commit in (0, 1):
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        S = x["h0"].clone()
+        kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, commit=bool(commit),
+                             status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) & kda.KDA_DEV_NONFINITE

@@ -97,19 +97,61 @@ def test_segmented_status_flags():
     assert st & kda.KDA_DEV_DECAY_RANGE
 
 
-def test_segmented_t1m_against_single_pass():
-    """T = 2^20 over two heads, eight segments: the segmented result against
-    the single-pass kernel (the oracle covers the same heads in the
-    single-pass test). Differences are rounding: o of later segments is the
-    sum of two bf16-rounded parts."""
+@pytest.mark.parametrize("name", ["q", "k", "v"])
+def test_segmented_nonfinite_qkv_is_flagged(name):
+    x = inputs.prefill_inputs(workload(True), DEV, B=1, T=500, H=2, seed=16)
+    x[name][0, 300, 1, 90] = float("nan")  # in a later segment
+    _, _, st = run_seg(x, 3)
+    assert st & kda.KDA_DEV_NONFINITE
+
+
+@pytest.mark.slow
+def test_t1m_benchmark_calls_against_oracle():
+    """The long-context workload (B=1, T=2^20, H=32, the benchmark's seed)
+    through the two calls the benchmark times: kda_chunk_fwd in one pass and
+    kda_chunk_fwd_segmented with the segment count of
+    kda_chunk_fwd_segments_hint and the library's first-segment length. The
+    oracle recomputes four heads (two of them apart by half the head range)
+    over the whole sequence, and every output and the final state of those
+    heads is checked for both calls, so the transitions built over the long
+    segments are checked against the definition, not against the one-pass
+    kernel."""
     w = inputs.PREFILL_T1M
-    x = inputs.prefill_inputs(w, DEV, H=2)
-    o1, h1 = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None)
-    o2, h2, st = run_seg(dict(x, h0=None), 8)
-    assert st == 0
-    eo = o_err(o2, o1.double().cpu().numpy())
-    eh = s_err(h2, h1.double().cpu().numpy())
-    assert eo <= 2e-2 and eh <= 1e-2, (eo, eh)
+    x = inputs.prefill_inputs(w, DEV)
+    heads = [0, 11, 22, 31]
+    nseg = kda.kda_chunk_fwd_segments_hint(w.B, w.T, w.H, w.dk, w.dv)
+    assert nseg > 1
+    n_eff, sc, lead = kda.kda_chunk_fwd_segment_plan(w.B, w.T, w.H, w.dk, w.dv, nseg=nseg)
+    ws = torch.empty(kda.kda_chunk_fwd_segmented_workspace_size(w.B, w.T, w.H, w.dk, w.dv,
+                                                                nseg=nseg),
+                     dtype=torch.uint8, device=DEV)
+    o = torch.empty_like(x["v"])
+    hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = {}
+    kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, o=o, hT=hT,
+                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got["single"] = (o[:, :, heads].cpu(), hT[:, heads].cpu())
+    o.fill_(float("nan"))
+    hT.fill_(float("nan"))
+    kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], None, nseg=nseg,
+                                o=o, hT=hT, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got["segmented"] = (o[:, :, heads].cpu(), hT[:, heads].cpu())
+    sub = {n: x[n][:, :, heads].contiguous().cpu() for n in ("q", "k", "v", "g", "beta")}
+    del x, o, hT, ws
+    torch.cuda.empty_cache()
+    o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None,
+                                  nthreads=len(heads))
+    errs = {}
+    for name, (og, hg) in got.items():
+        errs[name] = (assert_o(og, o_ref, BF16, f"{name} o"),
+                      assert_s(hg, h_ref, BF16, f"{name} hT"))
+    print(f"\nT=2^20 H=32, heads {heads}: nseg {n_eff} (segment {sc} chunks, first {lead}x); "
+          + "; ".join(f"{n}: o {e[0]:.3e} hT {e[1]:.3e}" for n, e in errs.items()))
 
 
 def test_hint_and_workspace():
