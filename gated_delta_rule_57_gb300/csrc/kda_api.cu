@@ -410,6 +410,120 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
                           stream, nseg, ws, need > 0 ? sizeof(g_seg_scratch) : 0);
 }
 
+namespace {
+
+// Common checks of the two whole-slice passes: bf16, dk = dv = 128, inputs
+// present and aligned, `state` and `o` (either may be absent) clear of the
+// inputs and of each other.
+kda_status_t slice_args(const void* q, const void* k, const float* g, const float* beta,
+                        const void* state, size_t state_bytes, const void* o, int B, int T, int H,
+                        int dk, int dv, kda_dtype_t io, size_t* n_qk_out) {
+    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
+    kda_status_t st = check_dims(dk, dv, io);
+    if (st != KDA_OK) return st;
+    if (io != KDA_BF16 || dk != 128)
+        return fail(KDA_ERR_UNSUPPORTED, "slice passes need bf16 and dk = dv = 128");
+    if ((long long)B * H >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "B*H too large");
+    size_t n_qk, n_b, n_s;
+    if (!mul_ok(&n_qk, B, T, H, dk) || !mul_ok(&n_b, B, T, H) || !mul_ok(&n_s, B, H, dk, dv))
+        return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+    if (B == 0 || H == 0) return KDA_OK;
+    if (T > 0 && (!q || !k || !g || !beta))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, g and beta must be non-NULL");
+    if (!state) return fail(KDA_ERR_INVALID_ARG, "the state tensor must be non-NULL");
+    const void* ptrs[] = {q, k, g, state, o};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (beta && !aligned4(beta)) return fail(KDA_ERR_INVALID_ARG, "beta must be 4-byte aligned");
+    const void* ins[] = {q, k, g, beta};
+    const size_t in_bytes[] = {n_qk * 2, n_qk * 2, n_qk * 4, n_b * 4};
+    const size_t o_bytes = n_qk * 2;  // dv = dk
+    for (int i = 0; i < 4; i++) {
+        if (overlaps(state, state_bytes, ins[i], in_bytes[i]))
+            return fail(KDA_ERR_INVALID_ARG, "the state tensor overlaps an input");
+        if (overlaps(o, o_bytes, ins[i], in_bytes[i]))
+            return fail(KDA_ERR_INVALID_ARG, "o overlaps an input");
+    }
+    if (overlaps(o, o_bytes, state, state_bytes))
+        return fail(KDA_ERR_INVALID_ARG, "o overlaps the state tensor");
+    *n_qk_out = n_qk;
+    return KDA_OK;
+}
+
+}  // namespace
+
+kda_status_t kda_chunk_fwd_slice_transition(const void* q, const void* k, const float* g,
+                                            const float* beta, float* M, int B, int T, int H,
+                                            int dk, kda_dtype_t io, int* d_status,
+                                            void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd_slice_transition");
+    size_t n_qk = 0, n_m = 0;
+    if (B >= 0 && H >= 0 && dk > 0) mul_ok(&n_m, (size_t)B, (size_t)H, (size_t)dk, (size_t)dk);
+    kda_status_t st = slice_args(q, k, g, beta, M, n_m * 4, nullptr, B, T, H, dk, dk, io, &n_qk);
+    if (st != KDA_OK || B == 0 || H == 0) return st;
+    // v is not read (the run has v = 0); q stands in for its tensor map.
+    kda::ChunkFwdArgs a{q, k, q, g, beta, nullptr, nullptr, nullptr, B, T, H, dk, dk, d_status,
+                        static_cast<cudaStream_t>(stream)};
+    cudaError_t e = kda::launch_chunk_fwd_tc_slice(a, 1, M);
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+kda_status_t kda_chunk_fwd_slice_correct(const void* q, const void* k, const float* g,
+                                         const float* beta, const float* S_in, void* o, int B,
+                                         int T, int H, int dk, int dv, kda_dtype_t io,
+                                         int* d_status, void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd_slice_correct");
+    size_t n_qk = 0, n_s = 0;
+    if (B >= 0 && H >= 0 && dk > 0 && dv > 0)
+        mul_ok(&n_s, (size_t)B, (size_t)H, (size_t)dk, (size_t)dv);
+    kda_status_t st = slice_args(q, k, g, beta, S_in, n_s * 4, o, B, T, H, dk, dv, io, &n_qk);
+    if (st != KDA_OK || B == 0 || H == 0 || T == 0) return st;
+    if (!o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
+    kda::ChunkFwdArgs a{q, k, q, g, beta, nullptr, o, nullptr, B, T, H, dk, dv, d_status,
+                        static_cast<cudaStream_t>(stream)};
+    cudaError_t e = kda::launch_chunk_fwd_tc_slice(a, 2, const_cast<float*>(S_in));
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+kda_status_t kda_state_scan(const float* s0, const float* m, float* x_in, float* hT, int nslice,
+                            int B, int H, int dk, int dv, void* stream) {
+    NvtxRange nvtx_range("kda_state_scan");
+    if (nslice < 1 || B < 0 || H < 0)
+        return fail(KDA_ERR_INVALID_ARG, "nslice must be >= 1, B and H >= 0");
+    if (dk <= 0 || dv <= 0) return fail(KDA_ERR_INVALID_ARG, "dk and dv must be positive");
+    if (dk != 128 || dv != 128) return fail(KDA_ERR_UNSUPPORTED, "the scan needs dk = dv = 128");
+    if ((long long)B * H >= (1LL << 31)) return fail(KDA_ERR_INVALID_ARG, "B*H too large");
+    if (B == 0 || H == 0) return KDA_OK;
+    size_t n_s, n_all, n_rest;
+    if (!mul_ok(&n_s, B, H, dk, dv) || !mul_ok(&n_all, n_s, (size_t)nslice) ||
+        !mul_ok(&n_rest, n_s, (size_t)(nslice - 1)))
+        return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+    if (!s0 || (nslice > 1 && (!m || !x_in)))
+        return fail(KDA_ERR_INVALID_ARG, "s0, and for nslice > 1 m and x_in, must be non-NULL");
+    const void* ptrs[] = {s0, m, x_in, hT};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (overlaps(x_in, n_rest * 4, s0, n_all * 4) || overlaps(x_in, n_rest * 4, m, n_rest * 4) ||
+        overlaps(hT, n_s * 4, s0, n_all * 4) || overlaps(hT, n_s * 4, m, n_rest * 4) ||
+        overlaps(hT, n_s * 4, x_in, n_rest * 4))
+        return fail(KDA_ERR_INVALID_ARG, "outputs overlap the inputs or each other");
+    cudaError_t e = kda::launch_slice_scan(s0, m, x_in, hT, B * H, nslice,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 kda_status_t kda_selftest_wait_timeout(long long clocks, int* d_status, void* stream) {
     NvtxRange nvtx_range("kda_selftest_wait_timeout");
     if (clocks <= 0 || clocks > (1LL << 31))

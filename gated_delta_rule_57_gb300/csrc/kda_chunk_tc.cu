@@ -36,8 +36,11 @@
 // Thread 0 issues rounds 1, 3 and 4, a thread of warp 15 round 2; completion
 // is signalled through mbarriers whose waits are bounded (timeout ->
 // KDA_DEV_TIMEOUT). A CTA barrier stands only where a phase reads other warps'
-// results; round 1 waits on an arrive-only mbarrier instead, so the warps that
-// finish their operand rows first start their Gram-phase stores at once. Intermediates never leave the SM: the kernel reads each
+// results. The decay scan, the decay constants and the operand build need
+// none: each warp owns eight channels of all four tiles, so tile totals and
+// constants stay inside the warp. Round 1 waits on an arrive-only mbarrier,
+// so the warps that finish their operand rows first start their Gram-phase
+// stores at once. Intermediates never leave the SM: the kernel reads each
 // input once and writes o (and hT) once. The <true> instantiation also runs
 // the passes of the time-segmented evaluation (see TcParams).
 #include <cudaTypedefs.h>
@@ -59,7 +62,8 @@ constexpr int kRound2Thread = kThreads - 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (bytes from a 1024-aligned base).
-constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; then decay constants
+constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; then tile totals and
+                                       // decay constants (each warp in its own 8 channels' chunks)
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
 constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch
 constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
@@ -69,8 +73,7 @@ constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major A);
 constexpr uint32_t OFF_S = 188416;     // S0 bf16, SW128 128 x 128 (MN-major B)
 constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
 constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
-constexpr uint32_t OFF_GT = 221952;    // fp32 [4][128] tile log2-decay totals
-constexpr uint32_t SMEM_BYTES = 224000 + 1024;
+constexpr uint32_t SMEM_BYTES = 221952 + 1024;
 // U (64 x 128, MN-major B) reuses [Kt; Qt] once round 2 has completed.
 constexpr uint32_t OFF_U = OFF_AKQ;
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
@@ -109,6 +112,10 @@ struct TcParams {
     // last BH * (nseg - 1) CTAs run segments 1.. from the identity with v = 0,
     // leaving the segment transition in ws_m. Pass 2: segments 1.. again from
     // their incoming state ws_sin with v = 0, adding their outputs to o.
+    // Whole-slice passes (one CTA per sequence, all its chunks), for a
+    // sequence split across devices: pass 3 runs from the identity with
+    // v = 0 and writes the slice's transition to ws_m[bh]; pass 4 runs from
+    // ws_sin[bh] with v = 0 and adds its outputs to o.
     int pass, nseg, seg_chunks, lead, BH;
     float* ws_s0;         // [BH][nseg][dk][dv]
     float* ws_m;          // [BH][nseg - 1][dk][dk]
@@ -348,12 +355,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (its transition), kind 2 a segment from its incoming state with v = 0,
     // adding to o. Only kind and the first token stay live; the state
     // pointers are formed where they are used.
-    const int kind =
-        !SEG ? 0 : p.pass == 2 ? 2 : ((p.pass == 1 && (int)blockIdx.x >= p.BH * p.nseg) ? 1 : 0);
+    const int kind = !SEG                          ? 0
+                     : p.pass == 3                 ? 1
+                     : p.pass == 2 || p.pass == 4  ? 2
+                     : (p.pass == 1 && (int)blockIdx.x >= p.BH * p.nseg) ? 1
+                                                                          : 0;
     const bool v_zero = kind != 0;
+    const bool whole = !SEG || p.pass == 0 || p.pass >= 3;  // one CTA runs all the chunks
     auto task_seq = [&](int* bh_out, int* seg_out) {
         int bh = blockIdx.x, seg = 0;
-        if (kind == 2 || kind == 1) {
+        if (whole) {
+        } else if (kind == 2 || kind == 1) {
             const int j = kind == 1 ? (int)blockIdx.x - p.BH * p.nseg : (int)blockIdx.x;
             bh = j / (p.nseg - 1);
             seg = 1 + j % (p.nseg - 1);
@@ -371,17 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_begin = seg == 0 ? 0 : (p.lead + seg - 1) * p.seg_chunks * kC;
     // Initial state: h0 (whole sequences and first segments), zero (other
     // segments), the identity (transition runs) or the incoming state.
-    const float* h0p = kind == 2 ? p.ws_sin + ((size_t)bh * (p.nseg - 1) + seg - 1) * kD * kD
+    const float* h0p = (kind == 2 && whole) ? p.ws_sin + (size_t)bh * kD * kD
+                       : kind == 2 ? p.ws_sin + ((size_t)bh * (p.nseg - 1) + seg - 1) * kD * kD
                        : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * kD * kD
                                                          : nullptr;
-    const int nchunks = (!SEG || p.pass == 0)
+    const int nchunks = whole
                             ? (T + kC - 1) / kC
                             : min(seg == 0 ? p.lead * p.seg_chunks : p.seg_chunks,
                                   (T - t_begin + kC - 1) / kC);
     const uint32_t sbase = smem_addr(sm);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* slam = reinterpret_cast<float*>(sm + OFF_LAM);
-    float* sgt = reinterpret_cast<float*>(sm + OFF_GT);
     int flags = 0;
     bool failed = false;
 
@@ -437,6 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float beta_next = load_beta(0);
 
+    // T' is zero in the six 16 x 16 blocks above the diagonal; nothing else
+    // writes there, so they are cleared once.
+    for (int e = tid; e < 6 * 128; e += kThreads) {
+        const int blkid = e >> 7, i = (e >> 3) & 15, jp = e & 7;
+        const int br = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
+        const int bc = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
+        *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) =
+            0u;
+    }
     // Incoming state -> TMEM (lane i = key channel i, column j = value channel j).
     {
         const float* src = h0p ? h0p + (size_t)lane * kD + 32 * u : nullptr;
@@ -516,28 +537,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 stash[2][3];
         uint32_t p1_ro[2], p1_off;
         // ------------------------------------------------------------ P1
-        // Warp = (tile a, 32-channel block cb); lane = (row pair j, 8-channel
-        // group). Log-decays are kept in log2 units: each exponential is one ex2.
+        // Warp w owns channels 8w .. 8w + 7 of all four tiles; lane (a, j) =
+        // (lane / 8, lane % 8) owns rows 16a + j and 16a + j + 8 (so the 32
+        // lanes' row addresses cover all eight swizzle positions). Tile
+        // totals and decay constants never leave the warp: they go through
+        // the warp's own rows of the g buffer once its g values are read.
+        // Log-decays are kept in log2 units: each exponential is one ex2.
         bool ok = mbar_wait(&bars[BAR_QK], par) && mbar_wait(&bars[BAR_G], par);
+        if (!ok) flags |= KDA_DEV_TIMEOUT;  // voted on after the Gram readout
         {
-            const int a = warp >> 2, cb = warp & 3;
-            const int j = (tid & 31) >> 2, g8 = tid & 3;
-            const int c0 = cb * 32 + g8 * 8;
+            const int ln = tid & 31;
+            const int a = ln >> 3, j = ln & 7;
+            const int c0 = 8 * warp;
+            // this warp's 8 channels in the g buffer: block c0 / 32, chunks
+            // 2 (w % 4) and 2 (w % 4) + 1 of each 128-byte row (swizzled)
+            unsigned char* gblk = sm + OFF_G + (c0 >> 5) * 8192;
+            const uint32_t gch = 2u * (uint32_t)(warp & 3);
+            auto grow_chunk = [&](int r, int half) {
+                return gblk + r * 128 + (((gch + (uint32_t)half) ^ (uint32_t)(r & 7)) << 4);
+            };
             if (tid < kC) {
                 flags |= finite_flag(beta_next);
                 sbeta[tid] = beta_next;
             }
             beta_next = load_beta(c + 1);
-            float gam[2][8];  // in-tile inclusive cumulative log2-decay, rows 2j, 2j+1
+            float gam[2][8];  // in-tile inclusive cumulative log2-decay, rows j and j + 8
             float mn = 0.f, mx = -5.f, sum = 0.f;
 #pragma unroll
             for (int e = 0; e < 2; e++) {
-                const int r = 16 * a + 2 * j + e;
-                const unsigned char* grow = sm + OFF_G + cb * 8192 + r * 128;
+                const int r = 16 * a + j + 8 * e;
 #pragma unroll
                 for (int hq = 0; hq < 2; hq++) {
-                    const int chk = (2 * g8 + hq) ^ (r & 7);
-                    const float4 v = *reinterpret_cast<const float4*>(grow + chk * 16);
+                    const float4 v = *reinterpret_cast<const float4*>(grow_chunk(r, hq));
                     const float gv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int z = 0; z < 4; z++) {
@@ -550,61 +581,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!(fabsf(sum) <= 3.402823466e38f)) flags |= KDA_DEV_NONFINITE;
             else if (mn < kLogDecayMin || mx > 0.f) flags |= KDA_DEV_DECAY_RANGE;
-            // scan over the 8 row pairs of the tile (lanes g8, g8+4, ..., g8+28)
-            float tile_tot[8];  // inclusive sums: the tile totals in the last row pair (j = 7)
+            // Inclusive scans over the 8 lanes of the tile: rows j (e = 0) and
+            // j + 8 (e = 1, offset by the first half's total from lane j = 7).
 #pragma unroll
             for (int z = 0; z < 8; z++) {
-                gam[1][z] += gam[0][z];
-                float x = gam[1][z];
+                float x0 = gam[0][z], x1 = gam[1][z];
 #pragma unroll
                 for (int off = 1; off < 8; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, 4 * off);
-                    if (j >= off) x += y;
+                    const float y0 = __shfl_up_sync(0xffffffffu, x0, off, 8);
+                    const float y1 = __shfl_up_sync(0xffffffffu, x1, off, 8);
+                    if (j >= off) { x0 += y0; x1 += y1; }
                 }
-                const float excl = x - gam[1][z];
-                gam[0][z] += excl;
-                gam[1][z] += excl;
-                tile_tot[z] = x;
+                gam[0][z] = x0;
+                gam[1][z] = x1 + __shfl_sync(0xffffffffu, x0, 7, 8);
             }
+            __syncwarp();  // every lane has read its g values
+            // tile totals (lane j = 7 holds them in row j + 8 = 15) -> row 24 + a
             if (j == 7) {
-                *reinterpret_cast<float4*>(sgt + a * kD + c0) =
-                    make_float4(tile_tot[0], tile_tot[1], tile_tot[2], tile_tot[3]);
-                *reinterpret_cast<float4*>(sgt + a * kD + c0 + 4) =
-                    make_float4(tile_tot[4], tile_tot[5], tile_tot[6], tile_tot[7]);
+                *reinterpret_cast<float4*>(grow_chunk(24 + a, 0)) =
+                    make_float4(gam[1][0], gam[1][1], gam[1][2], gam[1][3]);
+                *reinterpret_cast<float4*>(grow_chunk(24 + a, 1)) =
+                    make_float4(gam[1][4], gam[1][5], gam[1][6], gam[1][7]);
             }
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            // Per (tile, channel) decay constants, once, into the (now free) g buffer:
+            __syncwarp();
+            // Per (tile, channel) decay constants; lane (a, j) computes those
+            // of tile a, channel c0 + j, into row 6a + k6:
             //   0: e^{G_a-}  1: e^{G_C - G_a+}  2: e^{tile total}  3..5: e^{G_{a'-} - G_a+}, a' = 1..3
-            float* CT = reinterpret_cast<float*>(sm + OFF_G);
             {
-                const int ta = tid >> 7, ch = tid & 127;
                 float tb[4];
 #pragma unroll
-                for (int bb = 0; bb < 4; bb++) tb[bb] = sgt[bb * kD + ch];
+                for (int bb = 0; bb < 4; bb++)
+                    tb[bb] = reinterpret_cast<const float*>(grow_chunk(24 + bb, j >> 2))[j & 3];
                 float pre = 0.f, post = 0.f, own = 0.f;
 #pragma unroll
                 for (int bb = 0; bb < 4; bb++) {
-                    if (bb < ta) pre += tb[bb];
-                    if (bb > ta) post += tb[bb];
-                    if (bb == ta) own = tb[bb];
+                    if (bb < a) pre += tb[bb];
+                    if (bb > a) post += tb[bb];
+                    if (bb == a) own = tb[bb];
                 }
-                CT[(ta * 6 + 0) * kD + ch] = fast_exp2(pre);
-                CT[(ta * 6 + 1) * kD + ch] = fast_exp2(post);
-                CT[(ta * 6 + 2) * kD + ch] = fast_exp2(own);
+                float cv[6];
+                cv[0] = fast_exp2(pre);
+                cv[1] = fast_exp2(post);
+                cv[2] = fast_exp2(own);
                 float run = 0.f;
 #pragma unroll
                 for (int ap = 1; ap < 4; ap++) {
-                    CT[(ta * 6 + 2 + ap) * kD + ch] = fast_exp2(run);
-                    if (ap > ta) run += tb[ap];
+                    cv[2 + ap] = fast_exp2(run);
+                    if (ap > a) run += tb[ap];
                 }
-                if (ta == 0) slam[ch] = fast_exp2(tb[0] + tb[1] + tb[2] + tb[3]);
+                if (a == 0) slam[c0 + j] = fast_exp2(tb[0] + tb[1] + tb[2] + tb[3]);
+#pragma unroll
+                for (int k6 = 0; k6 < 6; k6++)
+                    reinterpret_cast<float*>(grow_chunk(6 * a + k6, j >> 2))[j & 3] = cv[k6];
             }
-            __syncthreads();
+            __syncwarp();
             float cst[6][8];
 #pragma unroll
             for (int k6 = 0; k6 < 6; k6++) {
-                const float4 w0 = *reinterpret_cast<const float4*>(CT + (a * 6 + k6) * kD + c0);
-                const float4 w1 = *reinterpret_cast<const float4*>(CT + (a * 6 + k6) * kD + c0 + 4);
+                const float4 w0 = *reinterpret_cast<const float4*>(grow_chunk(6 * a + k6, 0));
+                const float4 w1 = *reinterpret_cast<const float4*>(grow_chunk(6 * a + k6, 1));
                 cst[k6][0] = w0.x; cst[k6][1] = w0.y; cst[k6][2] = w0.z; cst[k6][3] = w0.w;
                 cst[k6][4] = w1.x; cst[k6][5] = w1.y; cst[k6][6] = w1.z; cst[k6][7] = w1.w;
             }
@@ -613,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p1_off = blk * 8192u;
 #pragma unroll
             for (int e = 0; e < 2; e++) {
-                const int r = 16 * a + 2 * j + e;
+                const int r = 16 * a + j + 8 * e;
                 const uint32_t ro = (uint32_t)r * 128u + ((chunk ^ (uint32_t)(r & 7)) << 4);
                 unsigned char* pk = sm + OFF_KQP + blk * 16384u + ro;
                 unsigned char* pq = pk + 8192u;
@@ -699,6 +734,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tq + TM_S + 32 * u, y);
 #pragma unroll
             for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_S, lane, 32 * u + e, 128, y + e);
+            // e^{G_C} of this lane's key channel comes from another warp's
+            // decay constants, as does the beta the readout uses: every warp
+            // has arrived on BAR_P1 after writing them.
+            if (!mbar_wait(&bars[BAR_P1], par)) flags |= KDA_DEV_TIMEOUT;
             const float lam = slam[lane];
 #pragma unroll
             for (int e = 0; e < 32; e++) y[e] *= lam;
@@ -793,13 +832,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<__nv_bfloat16*>(TP + sw128_offset(o0 + i, o0 + jc, 128)) =
                             __float2bfloat16_rn(x[i] * bj);
                     }
-                }
-            } else if (warp < 15) {  // T' is zero in the six blocks above the diagonal
-                for (int e = tid - 128; e < 6 * 128; e += kThreads - 160) {
-                    const int blkid = e >> 7, i = (e >> 3) & 15, jp = e & 7;
-                    const int br = blkid < 3 ? 0 : (blkid < 5 ? 1 : 2);
-                    const int bc = blkid < 3 ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-                    *reinterpret_cast<uint32_t*>(TP + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) = 0u;
                 }
             }
             // Level 2 (warps 0-3) needs only the diagonal blocks of warps 0-3,
@@ -915,6 +947,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bh2, seg2;
         task_seq(&bh2, &seg2);
         if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * kD * kD : nullptr;
+        else if (p.pass == 3) hTp = p.ws_m + (size_t)bh2 * kD * kD;
+        else if (p.pass == 4) hTp = nullptr;
         else if (kind == 0) hTp = p.ws_s0 + ((size_t)bh2 * p.nseg + seg2) * kD * kD;
         else if (kind == 1) hTp = p.ws_m + ((size_t)bh2 * (p.nseg - 1) + seg2 - 1) * kD * kD;
     }
@@ -1011,6 +1045,18 @@ cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
     TcMaps m;
     if (!make_maps(&m, a)) return cudaErrorInvalidValue;
     return launch_tc<false>(m, base_params(a), (long long)a.B * a.H, a.stream);
+}
+
+cudaError_t launch_chunk_fwd_tc_slice(const ChunkFwdArgs& a, int which, float* state) {
+    TcMaps m;
+    if (!make_maps(&m, a)) return cudaErrorInvalidValue;
+    TcParams p = base_params(a);
+    p.hT = nullptr;
+    p.ckpt = nullptr;
+    p.pass = which == 1 ? 3 : 4;
+    if (which == 1) p.ws_m = state;
+    else p.ws_sin = state;
+    return launch_tc<true>(m, p, (long long)a.B * a.H, a.stream);
 }
 
 cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int seg_chunks,

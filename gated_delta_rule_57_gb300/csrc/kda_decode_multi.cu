@@ -31,7 +31,10 @@ namespace {
 
 constexpr int kStage = 8;  // tokens staged per pass
 
-template <typename TIn, int D>
+// WANT_O: outputs are computed (verify, or commit with o); without them the
+// reduction S^T (e^g q) is skipped. A verify leaves the state as it was, so
+// its last token's update is skipped too.
+template <typename TIn, int D, bool WANT_O>
 __global__ void __launch_bounds__(D, 384 / D)
     kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                             const TIn* __restrict__ v, const float* __restrict__ g,
@@ -111,10 +114,12 @@ __global__ void __launch_bounds__(D, 384 / D)
                     a[1] = fmaf(s4.y, lkv[rr], a[1]);
                     a[2] = fmaf(s4.z, lkv[rr], a[2]);
                     a[3] = fmaf(s4.w, lkv[rr], a[3]);
-                    bq[0] = fmaf(s4.x, lqv[rr], bq[0]);
-                    bq[1] = fmaf(s4.y, lqv[rr], bq[1]);
-                    bq[2] = fmaf(s4.z, lqv[rr], bq[2]);
-                    bq[3] = fmaf(s4.w, lqv[rr], bq[3]);
+                    if (WANT_O) {
+                        bq[0] = fmaf(s4.x, lqv[rr], bq[0]);
+                        bq[1] = fmaf(s4.y, lqv[rr], bq[1]);
+                        bq[2] = fmaf(s4.z, lqv[rr], bq[2]);
+                        bq[3] = fmaf(s4.w, lqv[rr], bq[3]);
+                    }
                 }
             }
             // totals over the four row groups (lanes l, l ^ 8, l ^ 16, l ^ 24)
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(D, 384 / D)
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     a[c] += __shfl_xor_sync(0xffffffffu, a[c], off);
-                    bq[c] += __shfl_xor_sync(0xffffffffu, bq[c], off);
+                    if (WANT_O) bq[c] += __shfl_xor_sync(0xffffffffu, bq[c], off);
                 }
             }
             float kq = 0.f;
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(D, 384 / D)
                 u[c] = bt * (vv[c] - a[c]);
                 ov[c] = bq[c] + u[c] * kq;
             }
-            if (o && rg == (tt & 3)) {  // the four row groups take turns storing
+            if (WANT_O && rg == (tt & 3)) {  // the four row groups take turns storing
                 TIn* dst = o + (((size_t)n * K + t0 + tt) * H + hh) * D + j;
                 if constexpr (sizeof(TIn) == 2) {
                     __nv_bfloat162 h0 = __floats2bfloat162_rn(ov[0], ov[1]);
@@ -151,6 +156,7 @@ __global__ void __launch_bounds__(D, 384 / D)
                     *reinterpret_cast<float4*>(dst) = make_float4(ov[0], ov[1], ov[2], ov[3]);
                 }
             }
+            if (!commit && t0 + tt + 1 == nt) break;  // a verify needs no state after its last token
             // S = Diag(e^g) S + k u^T
 #pragma unroll
             for (int r4 = 0; r4 < R; r4 += 4) {
@@ -179,10 +185,10 @@ __global__ void __launch_bounds__(D, 384 / D)
 template <typename TIn, int D>
 cudaError_t launch_t(const MultiDecodeArgs& a) {
     const unsigned grid = (unsigned)((long long)a.N * a.H);
-    kda_decode_multi_kernel<TIn, D><<<grid, D, 0, a.stream>>>(
-        static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
-        static_cast<const TIn*>(a.v), a.g, a.beta, a.S, static_cast<TIn*>(a.o), a.ntok, a.K,
-        a.H, a.commit, a.d_status);
+    auto kern = a.o ? kda_decode_multi_kernel<TIn, D, true> : kda_decode_multi_kernel<TIn, D, false>;
+    kern<<<grid, D, 0, a.stream>>>(static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
+                                   static_cast<const TIn*>(a.v), a.g, a.beta, a.S,
+                                   static_cast<TIn*>(a.o), a.ntok, a.K, a.H, a.commit, a.d_status);
     return cudaGetLastError();
 }
 

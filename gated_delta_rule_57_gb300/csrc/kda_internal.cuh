@@ -67,6 +67,17 @@ cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int s
                                           int lead, float* ws);
 cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                                 int nseg, cudaStream_t stream);
+// One time slice of every sequence (bf16, dk = dv = 128), for a sequence
+// split across devices: which = 1 writes the slice's transition (the run
+// from the identity with v = 0) to state [B*H][dk][dk]; which = 2 runs from
+// the incoming states `state` [B*H][dk][dv] with v = 0 and adds its outputs
+// to o. a.v is not read.
+cudaError_t launch_chunk_fwd_tc_slice(const ChunkFwdArgs& a, int which, float* state);
+// Scan over nslice slices stored slice-major: s0 [nslice][BH], m [nslice - 1][BH]
+// (the transitions of slices 1..), sin [nslice - 1][BH] (incoming states of
+// slices 1..), hT [BH] (nullable).
+cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
+                              int nslice, cudaStream_t stream);
 inline size_t segmented_workspace_floats(long long BH, int nseg) {
     // per sequence: nseg zero-start final states, nseg - 1 transitions and
     // nseg - 1 incoming states, 128 x 128 fp32 each

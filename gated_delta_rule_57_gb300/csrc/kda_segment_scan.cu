@@ -24,9 +24,19 @@ constexpr int kLd = kDs + 4;   // padded row: column reads of M fall on distinct
 constexpr int kScanThreads = 256;
 constexpr size_t kScanSmem = 2 * (size_t)kDs * kLd * sizeof(float);
 
+// Entry s of sequence bh sits at s0 + (s * s_seg + bh * s_bh) * DD, and
+// likewise for m and sin with their own strides (m and sin start at segment 1):
+// segment-major within a sequence (the time-segmented prefill) or sequence-
+// major within a segment (summaries gathered from the ranks of a sequence
+// split across devices).
+struct ScanLayout {
+    long long s0_seg, s0_bh, m_seg, m_bh, in_seg, in_bh;
+};
+
 __global__ void __launch_bounds__(kScanThreads)
     kda_segment_scan_kernel(const float* __restrict__ s0, const float* __restrict__ m,
-                            float* __restrict__ sin, float* __restrict__ hT, int nseg) {
+                            float* __restrict__ sin, float* __restrict__ hT, int nseg,
+                            const ScanLayout L) {
     extern __shared__ __align__(16) float smem[];
     float* X = smem;              // [kDs][kLd]
     float* Ms = smem + kDs * kLd;  // [kDs][kLd]
@@ -44,13 +54,17 @@ __global__ void __launch_bounds__(kScanThreads)
             if (copy_to) *reinterpret_cast<float4*>(copy_to + (size_t)r * kDs + 4 * c4) = f;
         }
     };
+    auto s0_at = [&](int s) { return s0 + ((long long)s * L.s0_seg + (long long)bh * L.s0_bh) * DD; };
+    auto m_at = [&](int s) { return m + ((long long)(s - 1) * L.m_seg + (long long)bh * L.m_bh) * DD; };
+    auto in_at = [&](int s) { return sin + ((long long)(s - 1) * L.in_seg + (long long)bh * L.in_bh) * DD; };
     // X_1 = S0_0, the incoming state of segment 1 (entry 0 of sin)
-    load(X, s0 + bh * nseg * DD, sin + bh * (nseg - 1) * DD);
+    load(X, s0_at(0), nseg > 1 ? in_at(1) : nullptr);
+    if (nseg == 1 && hT) load(X, s0_at(0), hT + bh * DD);
     for (int s = 1; s < nseg; s++) {
-        load(Ms, m + (bh * (nseg - 1) + s - 1) * DD, nullptr);
+        load(Ms, m_at(s), nullptr);
         __syncthreads();
         float acc[8][8];
-        const float* s0s = s0 + (bh * nseg + s) * DD;
+        const float* s0s = s0_at(s);
 #pragma unroll
         for (int a = 0; a < 8; a++) {
 #pragma unroll
@@ -74,7 +88,7 @@ __global__ void __launch_bounds__(kScanThreads)
             }
         }
         __syncthreads();  // every thread is done reading X and M
-        float* out = s + 1 < nseg ? sin + (bh * (nseg - 1) + s) * DD : (hT ? hT + bh * DD : nullptr);
+        float* out = s + 1 < nseg ? in_at(s + 1) : (hT ? hT + bh * DD : nullptr);
 #pragma unroll
         for (int a = 0; a < 8; a++) {
 #pragma unroll
@@ -90,14 +104,26 @@ __global__ void __launch_bounds__(kScanThreads)
 
 }  // namespace
 
-cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
-                                int nseg, cudaStream_t stream) {
+static cudaError_t launch_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
+                               int nseg, const ScanLayout& L, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kScanSmem);
     if (e != cudaSuccess) return e;
-    kda_segment_scan_kernel<<<BH, kScanThreads, kScanSmem, stream>>>(s0, m, sin, hT, nseg);
+    kda_segment_scan_kernel<<<BH, kScanThreads, kScanSmem, stream>>>(s0, m, sin, hT, nseg, L);
     return cudaGetLastError();
+}
+
+cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
+                                int nseg, cudaStream_t stream) {
+    const ScanLayout L{1, nseg, 1, nseg - 1, 1, nseg - 1};
+    return launch_scan(s0, m, sin, hT, BH, nseg, L, stream);
+}
+
+cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
+                              int nslice, cudaStream_t stream) {
+    const ScanLayout L{BH, 1, BH, 1, BH, 1};
+    return launch_scan(s0, m, sin, hT, BH, nslice, L, stream);
 }
 
 }  // namespace kda

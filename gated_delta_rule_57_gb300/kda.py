@@ -94,6 +94,14 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.kda_chunk_fwd_segment_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
                                                      ctypes.POINTER(I)]
             L.kda_chunk_fwd_segment_plan.restype = I
+            L.kda_chunk_fwd_slice_transition.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp,
+                                                         vp]
+            L.kda_chunk_fwd_slice_transition.restype = I
+            L.kda_chunk_fwd_slice_correct.argtypes = [vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, vp,
+                                                      vp]
+            L.kda_chunk_fwd_slice_correct.restype = I
+            L.kda_state_scan.argtypes = [vp, vp, vp, vp, I, I, I, I, I, vp]
+            L.kda_state_scan.restype = I
             L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp, vp]
             L.kda_decode_step.restype = I
             L.kda_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I,
@@ -241,6 +249,51 @@ def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, h0=None, *, nseg: int, o=N
                                                  nseg, _ptr(status), _stream(stream))
     _check(code)
     return o, hT
+
+
+def kda_chunk_fwd_slice_transition(q, k, g, beta, *, M=None,
+                                   status: Optional[torch.Tensor] = None, stream=None):
+    """Transition of one time slice: M [B,H,dk,dk] = product of the slice's
+    per-token transitions (the recurrence from the identity with v = 0)."""
+    B, T, H, dk = q.shape
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    if M is None:
+        M = torch.empty((B, H, dk, dk), dtype=torch.float32, device=q.device)
+    _check(lib().kda_chunk_fwd_slice_transition(_ptr(q), _ptr(k), _ptr(g), _ptr(beta), _ptr(M),
+                                                B, T, H, dk, io, _ptr(status), _stream(stream)))
+    return M
+
+
+def kda_chunk_fwd_slice_correct(q, k, g, beta, S_in, o, *,
+                                status: Optional[torch.Tensor] = None, stream=None):
+    """o += the outputs the incoming state S_in [B,H,dk,dv] contributes over
+    the slice (the recurrence from S_in with v = 0). Returns o."""
+    B, T, H, dk = q.shape
+    dv = o.shape[-1]
+    io = _DTYPE.get(q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported q dtype {q.dtype}")
+    _check(lib().kda_chunk_fwd_slice_correct(_ptr(q), _ptr(k), _ptr(g), _ptr(beta), _ptr(S_in),
+                                             _ptr(o), B, T, H, dk, dv, io, _ptr(status),
+                                             _stream(stream)))
+    return o
+
+
+def kda_state_scan(s0, m=None, *, x_in=None, hT=None, want_hT: bool = True, stream=None):
+    """Prefix scan over slice summaries: s0 [n,B,H,dk,dv] (zero-start final
+    states; slice 0's from the true initial state), m [n-1,B,H,dk,dk]
+    (transitions of slices 1..). Returns (x_in [n-1,B,H,dk,dv] incoming
+    states of slices 1.., hT [B,H,dk,dv])."""
+    n, B, H, dk, dv = s0.shape
+    if x_in is None and n > 1:
+        x_in = torch.empty((n - 1, B, H, dk, dv), dtype=torch.float32, device=s0.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=s0.device)
+    _check(lib().kda_state_scan(_ptr(s0), _ptr(m), _ptr(x_in), _ptr(hT), n, B, H, dk, dv,
+                                _stream(stream)))
+    return x_in, hT
 
 
 def kda_selftest_wait_timeout(status: torch.Tensor, clocks: int = 1 << 20, stream=None):

@@ -250,6 +250,62 @@ int kda_chunk_fwd_segment_plan(int B, int T, int H, int dk, int dv, kda_dtype_t 
                                int* seg_chunks, int* lead);
 
 /*
+ * Building blocks for one long sequence split in time across devices (or
+ * processes): section "The bill arrives in the serving stack", first bullet,
+ * of the orkas.ai page "Kimi K3 architecture". The incoming state of a later
+ * time slice is not a sum of per-slice states, but every slice has two
+ * composable summaries: its cumulative transition M (the product of its
+ * per-token transitions (I - b k k^T) Diag(e^g)) and its final state S0 from a
+ * zero start; a prefix scan over them rebuilds every slice's incoming state
+ * after one fixed-size exchange of the summaries. With the time slices
+ * numbered 0 .. n-1, each on its own device:
+ *   1. kda_chunk_fwd on the slice (slice 0 from h0, the others from zero)
+ *      writes o and S0; kda_chunk_fwd_slice_transition writes M (slices > 0);
+ *   2. the (S0, M) pairs of all slices are gathered on every device;
+ *   3. kda_state_scan turns them into the incoming state of every slice and
+ *      the sequence's final state;
+ *   4. kda_chunk_fwd_slice_correct adds, on slices > 0, the outputs that the
+ *      incoming state contributes.
+ * The package's seqsplit.py runs these steps over a torch.distributed group.
+ * All three need io = KDA_BF16 and dk = dv = 128 (KDA_ERR_UNSUPPORTED
+ * otherwise); tensors as for kda_chunk_fwd, [B, T, H, dk] for the slice.
+ */
+
+/*
+ * M[b, h] = the product of the slice's per-token transitions (the recurrence
+ * run from the identity with v = 0): [B, H, dk, dk] fp32, out, must not
+ * overlap the inputs; the identity when T = 0. q and k are of type io; g and
+ * beta fp32. d_status and stream as for kda_chunk_fwd.
+ */
+kda_status_t kda_chunk_fwd_slice_transition(const void* q, const void* k, const float* g,
+                                            const float* beta, float* M, int B, int T, int H,
+                                            int dk, kda_dtype_t io, int* d_status, void* stream);
+
+/*
+ * o += the outputs of the recurrence over the slice run from S_in with v = 0,
+ * i.e. what the slice's incoming state adds to the outputs of its zero-start
+ * run. S_in: [B, H, dk, dv] fp32 (in); o: [B, T, H, dv] of type io (in/out,
+ * must not overlap the inputs or S_in). Other arguments as above.
+ */
+kda_status_t kda_chunk_fwd_slice_correct(const void* q, const void* k, const float* g,
+                                         const float* beta, const float* S_in, void* o, int B,
+                                         int T, int H, int dk, int dv, kda_dtype_t io,
+                                         int* d_status, void* stream);
+
+/*
+ * Prefix scan over the summaries of nslice consecutive time slices, all fp32:
+ *   s0   : [nslice, B, H, dk, dv]      final states from a zero start (slice
+ *                                      0's from the sequence's initial state)
+ *   m    : [nslice - 1, B, H, dk, dk]  transitions of slices 1 .. nslice - 1
+ *   x_in : [nslice - 1, B, H, dk, dv]  out: incoming state of slices 1 ..
+ *   hT   : [B, H, dk, dv] or NULL      out: the sequence's final state
+ * X_1 = s0[0], X_{s+1} = s0[s] + m[s - 1] X_s. m and x_in may be NULL when
+ * nslice = 1. Outputs must not overlap the inputs or each other.
+ */
+kda_status_t kda_state_scan(const float* s0, const float* m, float* x_in, float* hT, int nslice,
+                            int B, int H, int dk, int dv, void* stream);
+
+/*
  * Self-test of failure detection. Every wait of the kernels above on an
  * mbarrier (TMA arrival, MMA completion) is a bounded loop: when it gives up
  * (~2^31 SM clocks) the kernel ORs KDA_DEV_TIMEOUT into *d_status, stops, frees
