@@ -92,7 +92,7 @@ static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 ==
 // TMEM columns.
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
 
-enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, BAR_P1 = 6, NBAR = 7 };
+enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, BAR_P1 = 6, BAR_GP = 7, NBAR = 8 };
 
 struct TcParams {
     const float* beta;
@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t bars[NBAR];
     __shared__ uint32_t tmem_slot;
+    // Runs with v = 0 (transitions, corrections): some lane of the incoming
+    // state of the chunk of parity p is nonzero.
+    __shared__ int s_nz[2];
 
     const int tid = threadIdx.x, warp = tid >> 5;
     // TMEM view of a warp: lane quarter q (lanes 32q..32q+31), column group u.
@@ -395,10 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* slam = reinterpret_cast<float*>(sm + OFF_LAM);
     int flags = 0;
-    bool failed = false;
+    bool failed = false, zero_exit = false;
 
     if (tid == 0) {
-        for (int i = 0; i < NBAR; i++) mbar_init(&bars[i], i == BAR_P1 ? kThreads : 1);
+        s_nz[0] = s_nz[1] = 0;
+        for (int i = 0; i < NBAR; i++)
+            mbar_init(&bars[i], (i == BAR_P1 || i == BAR_GP) ? kThreads : 1);
         fence_mbarrier_init();
         if (nchunks > 0) {
             prefetch_tensormap(&map_q);
@@ -732,6 +737,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM.
             float y[32];
             tmem_ld32(tq + TM_S + 32 * u, y);
+            if (SEG && v_zero) {
+                bool nz = false;
+#pragma unroll
+                for (int e = 0; e < 32; e++) nz = nz || (y[e] != 0.f);  // NaN counts as nonzero
+                if (__any_sync(0xffffffffu, nz) && (tid & 31) == 0) s_nz[par] = 1;
+            }
 #pragma unroll
             for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_S, lane, 32 * u + e, 128, y + e);
             // e^{G_C} of this lane's key channel comes from another warp's
@@ -746,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
         }
         fence_proxy_async_smem();
+        mbar_arrive(&bars[BAR_GP]);  // stash stores and the S0 copy are in shared memory
         ok = mma_wait() && ok;
         tc_fence_after();
         // Each warp waited for the Gram round itself; the next q, k tiles may
@@ -793,7 +805,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (SEG) {  // the segment passes decide on an early stop here: a CTA barrier
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        } else {
+            if (!ok) flags |= KDA_DEV_TIMEOUT;  // voted on at the end of the solve
+            // The solve reads A rows written by warps 0, 1, 4, 5 (synced here), 9,
+            // 13, and its level-3 slabs reuse rows that warps 8, 12 write.
+            if (warp < 8) named_sync(3, 384);
+            else if (q < 2) asm volatile("bar.arrive 3, 384;" ::: "memory");
+        }
+        if (SEG && v_zero && s_nz[par] == 0) {
+            // With v = 0 and an incoming state that is exactly zero in fp32,
+            // every later state and output of the run is exactly zero: the
+            // transition is zero and nothing more is added to o. The run
+            // stops here, once the tiles already requested have landed.
+            zero_exit = true;
+            if (tid == 0 && c + 1 < nchunks) {
+                const uint32_t np = (uint32_t)((c + 1) & 1);
+                if (!mbar_wait(&bars[BAR_QK], np) || !mbar_wait(&bars[BAR_G], np))
+                    flags |= KDA_DEV_TIMEOUT;
+            }
+            break;
+        }
 
         // ------------------------------------------------------------ T = (I + A)^-1
         {
@@ -803,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char* TP = sm + OFF_A0;  // T' rows 0..63
             if (tid == kRound2Thread) {
                 // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
+                if (!mbar_wait(&bars[BAR_GP], par)) flags |= KDA_DEV_TIMEOUT;
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
                 const uint64_t ad0 = desc_kmajor(sbase + OFF_AKQ);
@@ -870,7 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (__syncthreads_or(!ok || (flags & KDA_DEV_TIMEOUT))) { failed = true; break; }
+        if (SEG && tid == 0) s_nz[par] = 0;  // every thread has read it
 
         // ------------------------------------------------------------ round 3: U = T' V'
         if (tid == 0) {
@@ -937,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed && r4_pending && __syncthreads_or(!r4_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
-    if (nchunks > 0 && !failed && q >= 2)
+    if (nchunks > 0 && !failed && !zero_exit && q >= 2)
         store_o(nchunks - 1, min(kC, T - t_begin - (nchunks - 1) * kC));
     // Final state -> hT.
     // Final state: hT (whole sequences), the segment's zero-start state or
