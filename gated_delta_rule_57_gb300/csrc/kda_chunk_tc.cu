@@ -90,7 +90,7 @@ static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 ==
               "ldmatrix rows must start on 16-byte boundaries");
 
 // TMEM columns.
-constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_AUX = 416, TM_COLS = 512;
 
 enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, BAR_P1 = 6, BAR_GP = 7, NBAR = 8 };
 
@@ -168,6 +168,28 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va,
         vb[i] = __uint_as_float(r[16 + i]);
     }
 }
+
+// D[tmem] (+)= A[tmem] * B[smem]: A is M lanes x K, two bf16 per 32-bit column
+// (k = 2c in the low half of column c), so a K = 16 step advances 8 columns.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+        : "memory");
+}
+// Two bf16 (a in the low half) as the fp32 bit pattern tcgen05.st takes.
+__device__ __forceinline__ float pack2f(float a, float b) { return __uint_as_float(pack_bf16(a, b)); }
 
 // CTA barrier among `count` threads (whole warps) on named barrier `id` (1..15).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
@@ -463,53 +485,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) =
             0u;
     }
-    // Incoming state -> TMEM (lane i = key channel i, column j = value channel j).
+    // Incoming state -> TMEM, transposed: lane j = value channel j, column i
+    // = key channel i (a warp reads 128 contiguous bytes of a state row per load).
     {
-        const float* src = h0p ? h0p + (size_t)lane * kD + 32 * u : nullptr;
+        float x[32];
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 16) {
-            float x[16];
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                float4 f = src ? *reinterpret_cast<const float4*>(src + cc + j)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                x[j] = f.x; x[j + 1] = f.y; x[j + 2] = f.z; x[j + 3] = f.w;
-            }
-            if (kind == 1) {
-#pragma unroll
-                for (int j = 0; j < 16; j++) x[j] = (lane == 32 * u + cc + j) ? 1.f : 0.f;
-            }
-            tmem_st16(tq + TM_S + 32 * u + cc, x);
+        for (int e = 0; e < 32; e++) {
+            const int i = 32 * u + e;
+            x[e] = kind == 1 ? (lane == i ? 1.f : 0.f) : (h0p ? h0p[(size_t)i * kD + lane] : 0.f);
         }
+        tmem_st16(tq + TM_S + 32 * u, x);
+        tmem_st16(tq + TM_S + 32 * u + 16, x + 16);
         tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // O rows of chunk cc (D1 lanes 64..127, columns [32u, 32u + 32)) -> global.
+    // O of chunk cc -> global: O^T sits in D1 columns 64 + r (token r), lane j
+    // (value channel j); warp column group u takes tokens [16u, 16u + 16), so a
+    // warp store covers 32 consecutive value channels of one token.
     auto store_o = [&](int cc, int len) {
         if (kind == 1) return;
-        float x[32];
-        tmem_ld32(tq + TM_D1 + 32 * u, x);
+        float x[16];
+        tmem_ld16(tq + TM_D1 + 64 + 16 * u, x);
         // A NaN or Inf in q, k or v reaches some output through the
         // recurrence; x * 0 is 0 for finite x and NaN otherwise.
-        float probe = 0.f;
+        float pr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 32; e++) probe = fmaf(x[e], 0.f, probe);
-        if (probe != 0.f) flags |= KDA_DEV_NONFINITE;
-        if (lane - 64 < len) {
-            __nv_bfloat16* dst =
-                p.o + (((size_t)b * T + t_begin + cc * kC + lane - 64) * p.H + h) * kD + 32 * u;
+        for (int e = 0; e < 16; e++) pr[e & 3] = fmaf(x[e], 0.f, pr[e & 3]);
+        if ((pr[0] + pr[1]) + (pr[2] + pr[3]) != 0.f) flags |= KDA_DEV_NONFINITE;
+        __nv_bfloat16* dst = p.o + (((size_t)b * T + t_begin + cc * kC) * p.H + h) * kD + lane;
+        const size_t rs = (size_t)p.H * kD;
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-                if (kind == 2) {  // o += this pass's contribution
-                    float prev[8];
-                    unpack8(*reinterpret_cast<const uint4*>(dst + e), prev);
-#pragma unroll
-                    for (int z = 0; z < 8; z++) x[e + z] += prev[z];
-                }
-                *reinterpret_cast<uint4*>(dst + e) = pack8(x + e);
+        for (int e = 0; e < 16; e++) {
+            const int r = 16 * u + e;
+            if (r < len) {
+                float val = x[e];
+                if (kind == 2) val += __bfloat162float(dst[r * rs]);  // o += this pass's part
+                dst[r * rs] = __float2bfloat16_rn(val);
             }
         }
     };
@@ -670,8 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int z = 0; z < 8; z++) {
                     kp[z] = kf[z] * e1[z];
                     qp[z] = qf[z] * e1[z];
-                    ke[z] = kf[z] * (em[z] * cst[2][z]);  // k e^{G_a+ - G_r}, <= |k|
                     t8[z] = kf[z] * em[z];                // own window: bounded reciprocal decay
+                    ke[z] = t8[z] * cst[2][z];            // k e^{G_a+ - G_r}, <= |k|
                 }
                 *reinterpret_cast<uint4*>(pk) = pack8(kp);
                 *reinterpret_cast<uint4*>(pq) = pack8(qp);
@@ -732,9 +746,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(sm + OFF_KB + p1_off + p1_ro[e]) = stash[e][2];
         }
         // The previous (full) chunk's O rows, D1 lanes 64..127 -> global.
-        if (c > 0 && q >= 2 && ok) store_o(c - 1, kC);
+        if (c > 0 && ok) store_o(c - 1, kC);
         if (ok) {
-            // S0 (lane = key channel) -> bf16 operand copy; S <- e^{G_C} S in TMEM.
+            // S0^T (lane = value channel, columns = key channels 32u ..) -> bf16
+            // A operand of round 2 in TMEM; S <- e^{G_C} S (per key channel).
             float y[32];
             tmem_ld32(tq + TM_S + 32 * u, y);
             if (SEG && v_zero) {
@@ -743,21 +758,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; e++) nz = nz || (y[e] != 0.f);  // NaN counts as nonzero
                 if (__any_sync(0xffffffffu, nz) && (tid & 31) == 0) s_nz[par] = 1;
             }
+            {
+                float pk[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_S, lane, 32 * u + e, 128, y + e);
-            // e^{G_C} of this lane's key channel comes from another warp's
-            // decay constants, as does the beta the readout uses: every warp
-            // has arrived on BAR_P1 after writing them.
+                for (int e = 0; e < 16; e++) pk[e] = pack2f(y[2 * e], y[2 * e + 1]);
+                tmem_st16(tq + TM_AUX + 16 * u, pk);
+            }
+            // e^{G_C} of these key channels comes from other warps' decay
+            // constants, as does the beta the readout uses: every warp has
+            // arrived on BAR_P1 after writing them.
             if (!mbar_wait(&bars[BAR_P1], par)) flags |= KDA_DEV_TIMEOUT;
-            const float lam = slam[lane];
 #pragma unroll
-            for (int e = 0; e < 32; e++) y[e] *= lam;
+            for (int e = 0; e < 32; e += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(slam + 32 * u + e);
+                y[e] *= l4.x; y[e + 1] *= l4.y; y[e + 2] *= l4.z; y[e + 3] *= l4.w;
+            }
             tmem_st16(tq + TM_S + 32 * u, y);
             tmem_st16(tq + TM_S + 32 * u + 16, y + 16);
             tmem_wait_st();
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars[BAR_GP]);  // stash stores and the S0 copy are in shared memory
+        tc_fence_before();
+        mbar_arrive(&bars[BAR_GP]);  // stash stores in shared memory, S0^T copy in TMEM
         ok = mma_wait() && ok;
         tc_fence_after();
         // Each warp waited for the Gram round itself; the next q, k tiles may
@@ -838,13 +860,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
                 if (!mbar_wait(&bars[BAR_GP], par)) flags |= KDA_DEV_TIMEOUT;
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
-                const uint64_t ad0 = desc_kmajor(sbase + OFF_AKQ);
-                const uint64_t bd0 = desc_mnmajor(sbase + OFF_S, 128);
+                // D1^T: [Y^T | (Qt S0)^T] = S0^T [Kt; Qt]^T, A = S0^T in TMEM.
+                const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+                const uint64_t bd0 = desc_kmajor(sbase + OFF_AKQ);
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
-                    mma_bf16(tbase + TM_D1, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk),
-                             idesc, kk > 0);
+                    mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, bd0 + kstep_kmajor(128, kk),
+                                idesc, kk > 0);
                 mma_commit(&bars[BAR_R2]);
             }
             if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
@@ -876,28 +898,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             solve_level2(FA, FT, MS, warp, tid & 31, TP, sbeta);
             if (warp < 8) named_sync(2, 256);
             solve_level3(FA, FT, warp, tid & 31, TP, sbeta);
-            if (warp >= 8 && q < 2) {
-                // V' = V - Y for token rows lane (0..63), value columns [64 hv, 64 hv + 64),
-                // in place of v, by the four warps that are idle in this level.
+            if (warp >= 8) {
+                // -Y^T (D1 columns 0..63: tokens) -> bf16 A operand of round 3 in
+                // TMEM (AUX columns 0..31; S0^T there is consumed), tokens
+                // [32 (u - 2), + 32), by the eight warps idle in this level.
                 ok = v_zero || mbar_wait(&bars[BAR_V], par);
                 ok = mbar_wait(&bars[BAR_R2], r2_phase) && ok;
                 tc_fence_after();
-                const int hv = (warp >> 2) & 1;
                 if (ok) {
+                    const int t0 = 32 * (u - 2);
+                    float y[32], pk[16];
+                    tmem_ld32(tq + TM_D1 + t0, y);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; h2++) {
-                        const int c0 = 64 * hv + 32 * h2;
-                        float y[32];
-                        tmem_ld32(tq + TM_D1 + c0, y);
-#pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            float vv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            if (!v_zero) ld_row8(sm + OFF_V, lane, c0 + e, 64, vv);
-#pragma unroll
-                            for (int z = 0; z < 8; z++) vv[z] -= y[e + z];
-                            st_row8(sm + OFF_V, lane, c0 + e, 64, vv);
-                        }
-                    }
+                    for (int e = 0; e < 16; e++) pk[e] = pack2f(-y[2 * e], -y[2 * e + 1]);
+                    tmem_st16(tq + TM_AUX + t0 / 2, pk);
+                    tmem_wait_st();
                 }
             }
             r2_phase ^= 1u;
@@ -907,26 +922,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__syncthreads_or(!ok || (flags & KDA_DEV_TIMEOUT))) { failed = true; break; }
         if (SEG && tid == 0) s_nz[par] = 0;  // every thread has read it
 
-        // ------------------------------------------------------------ round 3: U = T' V'
+        // ------------------------------------------------------------ round 3: U^T = (V - Y)^T T'^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
-            const uint64_t ad0 = desc_kmajor(sbase + OFF_A0);  // [T'; P]
-            const uint64_t bd0 = desc_mnmajor(sbase + OFF_V, 64);
+            const uint32_t idesc_v = idesc_bf16(128, 64, 1, 0);  // A = v tile (MN-major)
+            const uint32_t idesc_y = idesc_bf16(128, 64, 0, 0);  // A = -Y^T (TMEM)
+            const uint64_t vd0 = desc_mnmajor(sbase + OFF_V, 64);
+            const uint64_t td0 = desc_kmajor(sbase + OFF_A0);    // T': rows 0..63 of [T'; P]
+            if (!v_zero) {
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++)
+                    mma_bf16(tbase + TM_D1, vd0 + kstep_mnmajor(kk), td0 + kstep_kmajor(128, kk),
+                             idesc_v, kk > 0);
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc,
-                         kk > 0);
+                mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, td0 + kstep_kmajor(128, kk),
+                            idesc_y, (!v_zero) || kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
         tc_fence_after();
         if (tid == 0 && c + 1 < nchunks && !v_zero) issue_v(c + 1);
-        if (q < 2) {  // U rows (scratch lanes 0..63) -> bf16 operand
-            float x[32];
-            tmem_ld32(tq + TM_SCR + 32 * u, x);
+        {  // U^T (D1 columns 16u .. + 16: tokens) -> bf16 A operand of round 4 in TMEM
+            float x[16], pk[8];
+            tmem_ld16(tq + TM_D1 + 16 * u, x);
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) st_row8(sm + OFF_U, lane, 32 * u + e, 64, x + e);
+            for (int e = 0; e < 8; e++) pk[e] = pack2f(x[2 * e], x[2 * e + 1]);
+            tmem_st8(tq + TM_AUX + 32 + 8 * u, pk);
+            tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -935,18 +959,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ round 4: S += Kb^T U, O += P U
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 128, 1, 1);
-            const uint64_t ad0 = desc_mnmajor(sbase + OFF_KB, 64);
-            const uint64_t bd0 = desc_mnmajor(sbase + OFF_U, 64);
+            // S^T += U^T Kb (B = Kb, MN-major), O^T += U^T P^T (B = P, K-major); A = U^T in TMEM
+            const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+            const uint64_t kb0 = desc_mnmajor(sbase + OFF_KB, 64);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_S, ad0 + kstep_mnmajor(kk), bd0 + kstep_mnmajor(kk), idesc, 1);
-            const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);
-            const uint64_t pd0 = desc_kmajor(sbase + OFF_A0);  // [T'; P]: rows 0..63 of D1 are dead
+                mma_bf16_ta(tbase + TM_S, tbase + TM_AUX + 32 + 8 * kk, kb0 + kstep_mnmajor(kk), idesc,
+                            1);
+            const uint32_t idesc_o = idesc_bf16(128, 64, 0, 0);
+            const uint64_t pd0 = desc_kmajor(sbase + OFF_A0 + 64 * 128);  // P: rows 64..127
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
-                mma_bf16(tbase + TM_D1, pd0 + kstep_kmajor(128, kk), bd0 + kstep_mnmajor(kk), idesc_o,
-                         1);
+                mma_bf16_ta(tbase + TM_D1 + 64, tbase + TM_AUX + 32 + 8 * kk,
+                            pd0 + kstep_kmajor(128, kk), idesc_o, 1);
             mma_commit(&bars[BAR_R4]);
         }
         r4_pending = true;
@@ -955,15 +980,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.ckpt && (c + 1) % p.ck_chunks == 0 && (c + 1) / p.ck_chunks <= p.n_ckpt) {
             if (__syncthreads_or(!r4_wait())) { failed = true; break; }
             const int jc = (c + 1) / p.ck_chunks - 1;
-            float* dst = p.ckpt + (((size_t)blockIdx.x * p.n_ckpt + jc) * kD + lane) * kD + 32 * u;
+            float* dst = p.ckpt + ((size_t)blockIdx.x * p.n_ckpt + jc) * kD * kD + lane;
 #pragma unroll
             for (int cc = 0; cc < 32; cc += 16) {
                 float x[16];
                 tmem_ld16(tq + TM_S + 32 * u + cc, x);
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 4)
-                    *reinterpret_cast<float4*>(dst + cc + jj) =
-                        make_float4(x[jj], x[jj + 1], x[jj + 2], x[jj + 3]);
+                for (int jj = 0; jj < 16; jj++) dst[(size_t)(32 * u + cc + jj) * kD] = x[jj];
             }
             tc_fence_before();
         }
@@ -972,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed && r4_pending && __syncthreads_or(!r4_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
-    if (nchunks > 0 && !failed && !zero_exit && q >= 2)
+    if (nchunks > 0 && !failed && !zero_exit)
         store_o(nchunks - 1, min(kC, T - t_begin - (nchunks - 1) * kC));
     // Final state -> hT.
     // Final state: hT (whole sequences), the segment's zero-start state or
@@ -988,15 +1011,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (kind == 1) hTp = p.ws_m + ((size_t)bh2 * (p.nseg - 1) + seg2 - 1) * kD * kD;
     }
     if (hTp && !failed) {
-        float* dst = hTp + (size_t)lane * kD + 32 * u;
+        float* dst = hTp + lane;
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 16) {
             float x[16];
             tmem_ld16(tq + TM_S + 32 * u + cc, x);
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4)
-                *reinterpret_cast<float4*>(dst + cc + jj) =
-                    make_float4(x[jj], x[jj + 1], x[jj + 2], x[jj + 3]);
+            for (int jj = 0; jj < 16; jj++) dst[(size_t)(32 * u + cc + jj) * kD] = x[jj];
         }
     }
     report_flags(p.d_status, flags);
