@@ -70,7 +70,7 @@ constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
 constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major A)
 constexpr uint32_t OFF_KB = 139264;    // Kb, SW128 64 x 128 (MN-major A)
 constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major A); then U
-constexpr uint32_t OFF_S = 188416;     // S0 bf16, SW128 128 x 128 (MN-major B)
+constexpr uint32_t OFF_KB1 = 188416;   // Kb of odd chunks (Kb of even chunks at OFF_KB)
 constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
 constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
 constexpr uint32_t SMEM_BYTES = 221952 + 1024;
@@ -553,8 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nchunks && !failed; c++) {
         const uint32_t par = (uint32_t)(c & 1);
 
-        uint4 stash[2][3];
-        uint32_t p1_ro[2], p1_off;
         // ------------------------------------------------------------ P1
         // Warp w owns channels 8w .. 8w + 7 of all four tiles; lane (a, j) =
         // (lane / 8, lane % 8) owns rows 16a + j and 16a + j + 8 (so the 32
@@ -664,7 +662,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t blk = (uint32_t)(c0 >> 6);
             const uint32_t chunk = (uint32_t)((c0 & 63) >> 3);
-            p1_off = blk * 8192u;
 #pragma unroll
             for (int e = 0; e < 2; e++) {
                 const int r = 16 * a + j + 8 * e;
@@ -699,18 +696,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4*>(pw + (uint32_t)win_row(ap) * 128u) = pack8(t8);
                     }
                 }
-                // Kt, Qt, Kb are not read by round 1: keep them (already
-                // rounded to bf16) and store them while round 1 runs.
-                p1_ro[e] = ro;
+                // Kt, Qt (round 2 of the previous chunk has read its copies) and
+                // Kb (into this chunk's parity buffer: round 4 of the previous
+                // chunk may still read the other).
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = kp[z] * cst[0][z];
-                stash[e][0] = pack8(t8);
+                *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * blk * 8192u + ro) = pack8(t8);
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = qp[z] * cst[0][z];
-                stash[e][1] = pack8(t8);
+                *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * blk * 8192u + 8192 + ro) = pack8(t8);
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = ke[z] * cst[1][z];
-                stash[e][2] = pack8(t8);
+                *reinterpret_cast<uint4*>(sm + (par ? OFF_KB1 : OFF_KB) + blk * 8192u + ro) =
+                    pack8(t8);
             }
         }
         // Only the Gram MMA and the next g load need every warp's operands
@@ -739,12 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // only ever set by a failed wait, so it fails the vote after the readout.)
         ok = r4_wait() && !(flags & KDA_DEV_TIMEOUT);
         if (!ok) flags |= KDA_DEV_TIMEOUT;
-#pragma unroll
-        for (int e = 0; e < 2; e++) {
-            *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * p1_off + p1_ro[e]) = stash[e][0];
-            *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * p1_off + 8192 + p1_ro[e]) = stash[e][1];
-            *reinterpret_cast<uint4*>(sm + OFF_KB + p1_off + p1_ro[e]) = stash[e][2];
-        }
         // The previous (full) chunk's O rows, D1 lanes 64..127 -> global.
         if (c > 0 && ok) store_o(c - 1, kC);
         if (ok) {
@@ -961,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // S^T += U^T Kb (B = Kb, MN-major), O^T += U^T P^T (B = P, K-major); A = U^T in TMEM
             const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
-            const uint64_t kb0 = desc_mnmajor(sbase + OFF_KB, 64);
+            const uint64_t kb0 = desc_mnmajor(sbase + (par ? OFF_KB1 : OFF_KB), 64);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16_ta(tbase + TM_S, tbase + TM_AUX + 32 + 8 * kk, kb0 + kstep_mnmajor(kk), idesc,
