@@ -18,31 +18,35 @@
 //   T' = (I + A)^-1 Diag(b),  Kt = k e^{G},  Qt = q e^{G},  Kb = k e^{G_C - G}
 //   W = T' Kt,  Ut = T' V,  U = Ut - W S0,  O = Qt S0 + P U,  S_C = Diag(e^{G_C}) S0 + Kb^T U.
 // Since W S0 = T' (Kt S0), the state enters only through Y = Kt S0 and
-// Qt S0, which need neither the Gram matrices nor the solve. As 128-row MMAs:
+// Qt S0, which need neither the Gram matrices nor the solve. The state is kept
+// transposed in tensor memory (lane = value channel j, column = key channel
+// i), so its bf16 copy, -Y and U serve as A operands straight from TMEM (two
+// bf16 per 32-bit column). As 128-row MMAs (D^T = A B^T):
 //   round 1  Gram blocks  [Kp; Qp] * [Km_0; Km_1; Km_2; Km_3]^T   (N = 16+32+48+64)
-//   round 2  D1  = [Kt; Qt] * S0                  -> [Y; Qt S0]   (runs under the solve)
-//            V'  = V - Y  (bf16, in place of v; under the solve as well)
-//   round 3  SCR = [T'; P] * V'                   -> [U; -]      (U = Ut - W S0)
-//   round 4  S  += Kb^T * U                       (S pre-scaled by e^{G_C} in TMEM)
-//            D1 += [T'; P] * U                    -> [-; O]      (O = Qt S0 + P U)
-// The O rows are read out while the next chunk's round 1 runs.
+//   round 2  D1 = S0^T [Kt; Qt]^T          -> [Y^T | (Qt S0)^T]  (A = S0^T in TMEM; under the solve)
+//            -Y^T -> bf16 A operand in TMEM (under the solve as well)
+//   round 3  D1[:, 0:64] = V^T T'^T + (-Y^T) T'^T -> U^T        (A = the v tile, MN-major; -Y^T)
+//   round 4  S^T += U^T Kb                 (S^T pre-scaled by e^{G_C} per key channel)
+//            D1[:, 64:128] += U^T P^T      -> O^T = (Qt S0 + P U)^T   (A = U^T in TMEM)
+// O^T is read out (a warp store covers 32 value channels of one token) while
+// the next chunk's round 1 runs.
 //
 // Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
-// lane quarter), ~220 KB of shared memory (one CTA per SM), 416 TMEM columns:
-// the fp32 state S (128 lanes x 128 columns) stays in tensor memory for the
-// whole sequence. Inputs arrive by TMA with the 128-byte swizzle (q, k, v in
-// the layout the MMA descriptors expect; g in 32-channel blocks); the next
-// chunk's g, q/k, v and beta are prefetched as soon as their buffers are free.
-// Thread 0 issues rounds 1, 3 and 4, a thread of warp 15 round 2; completion
-// is signalled through mbarriers whose waits are bounded (timeout ->
-// KDA_DEV_TIMEOUT). A CTA barrier stands only where a phase reads other warps'
-// results. The decay scan, the decay constants and the operand build need
-// none: each warp owns eight channels of all four tiles, so tile totals and
-// constants stay inside the warp. Round 1 waits on an arrive-only mbarrier,
-// so the warps that finish their operand rows first start their Gram-phase
-// stores at once. Intermediates never leave the SM: the kernel reads each
-// input once and writes o (and hT) once. The <true> instantiation also runs
-// the passes of the time-segmented evaluation (see TcParams).
+// lane quarter), ~220 KB of shared memory (one CTA per SM), 480 TMEM columns:
+// the fp32 state stays in tensor memory for the whole sequence. Inputs arrive
+// by TMA with the 128-byte swizzle (q, k, v in the layout the MMA descriptors
+// expect; g in 32-channel blocks); the next chunk's g, q/k, v and beta are
+// prefetched as soon as their buffers are free. Thread 0 issues rounds 1, 3
+// and 4, a thread of warp 15 round 2; completion is signalled through
+// mbarriers whose waits are bounded (timeout -> KDA_DEV_TIMEOUT). A CTA
+// barrier stands only where a phase reads other warps' results. The decay
+// scan, the decay constants and the operand build need none: each warp owns
+// eight channels of all four tiles, so tile totals and constants stay inside
+// the warp, and it stores its Kt, Qt and Kb rows as it builds them. Round 1
+// waits on an arrive-only mbarrier. Intermediates never leave the SM: the
+// kernel reads each input once and writes o (and hT) once. The <true>
+// instantiation also runs the passes of the time-segmented evaluation and of
+// a sequence split across devices (see TcParams).
 #include <cudaTypedefs.h>
 
 #include "kda_internal.cuh"
@@ -66,16 +70,14 @@ constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; the
                                        // decay constants (each warp in its own 8 channels' chunks)
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
 constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch
-constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major B)
-constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major A)
-constexpr uint32_t OFF_KB = 139264;    // Kb, SW128 64 x 128 (MN-major A)
-constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major A); then U
-constexpr uint32_t OFF_KB1 = 188416;   // Kb of odd chunks (Kb of even chunks at OFF_KB)
+constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major A of round 3)
+constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major B of rounds 3, 4)
+constexpr uint32_t OFF_KB = 139264;    // Kb of even chunks, SW128 64 x 128 (MN-major B)
+constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major B of round 2)
+constexpr uint32_t OFF_KB1 = 188416;   // Kb of odd chunks
 constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
 constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
 constexpr uint32_t SMEM_BYTES = 221952 + 1024;
-// U (64 x 128, MN-major B) reuses [Kt; Qt] once round 2 has completed.
-constexpr uint32_t OFF_U = OFF_AKQ;
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
 // the solve)
 constexpr int LDA = 68;  // fp32 A: TF32 fragment loads (bank 4g + t) and float4 row stores conflict-free
@@ -89,7 +91,9 @@ static_assert(OFF_MS + 4 * 128 * 4 <= OFF_V, "solve scratch overflows the window
 static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 == 0,
               "ldmatrix rows must start on 16-byte boundaries");
 
-// TMEM columns.
+// TMEM columns: the transposed state, round 2/3/4 accumulators (D1), the
+// Gram round's accumulator (SCR), and bf16 A operands (AUX: S0^T, then -Y^T
+// in columns 0..31 and U^T in 32..63).
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_AUX = 416, TM_COLS = 512;
 
 enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, BAR_P1 = 6, BAR_GP = 7, NBAR = 8 };
@@ -200,11 +204,6 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
 __device__ __forceinline__ void st_row8(unsigned char* tile, int r, int c0, int R,
                                         const float* x) {
     *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0, R)) = pack8(x);
-}
-
-__device__ __forceinline__ void ld_row8(const unsigned char* tile, int r, int c0, int R,
-                                        float* x) {
-    unpack8(*reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0, R)), x);
 }
 
 // Descriptors for the two operand orientations of an SW128 tile with R rows;
@@ -867,10 +866,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; i++) acc[i] = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; m++) {  // right-looking: finish x_m, push into later rows
-                    x[m] = (m < jc) ? 0.f : ((m == jc) ? 1.f : -acc[m]);
+                for (int m0 = 0; m0 < 16; m0 += 4) {  // right-looking, four columns of A per load
+                    float4 arow[16];
 #pragma unroll
-                    for (int i = m + 1; i < 16; i++) acc[i] += FA[(o0 + i) * LDA + o0 + m] * x[m];
+                    for (int i = m0 + 1; i < 16; i++)
+                        arow[i] = *reinterpret_cast<const float4*>(FA + (o0 + i) * LDA + o0 + m0);
+#pragma unroll
+                    for (int mm = 0; mm < 4; mm++) {  // finish x_m, push into later rows
+                        const int m = m0 + mm;
+                        x[m] = (m < jc) ? 0.f : ((m == jc) ? 1.f : -acc[m]);
+#pragma unroll
+                        for (int i = m + 1; i < 16; i++) {
+                            const float am = mm == 0 ? arow[i].x : mm == 1 ? arow[i].y
+                                           : mm == 2 ? arow[i].z : arow[i].w;
+                            acc[i] += am * x[m];
+                        }
+                    }
                 }
                 if ((tid & 31) < 16) {
                     const float bj = sbeta[o0 + jc];
