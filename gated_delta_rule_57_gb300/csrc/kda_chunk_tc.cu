@@ -63,6 +63,8 @@ constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
 // Round 2 is issued by warp 15, which has no other work during the solve
 // (issuing keeps a thread busy for about the MMA's duration).
 constexpr int kRound2Thread = kThreads - 32;
+// The next chunk's q/k and v tiles are requested by warp 10, idle in the solve.
+constexpr int kTmaThread = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (bytes from a 1024-aligned base).
@@ -718,7 +720,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ round 1: Gram
         if (tid == 0) {
             if (!mbar_wait(&bars[BAR_P1], par)) flags |= KDA_DEV_TIMEOUT;
-            if (c + 1 < nchunks) issue_g(c + 1);
             tc_fence_after();
             // The four windows are consecutive rows of one tile, so a single
             // N = 160 product computes every Gram block: columns win_row(a)..
@@ -731,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(tbase + TM_SCR, ad0 + kstep_kmajor(128, kk), bd0 + kstep_kmajor(KM_ROWS, kk),
                          idesc, kk > 0);
             mma_commit(&bars[BAR_MMA]);
+            if (c + 1 < nchunks) issue_g(c + 1);  // every warp is done with the g buffer
         }
         // Kb, U (under [Kt; Qt]), D1 and S are free again. (A timeout flag is
         // only ever set by a failed wait, so it fails the vote after the readout.)
@@ -775,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // Each warp waited for the Gram round itself; the next q, k tiles may
         // land as soon as it is done. A failure is voted on after the readout.
-        if (tid == 0 && c + 1 < nchunks) issue_qk(c + 1);
+        if (tid == kTmaThread && c + 1 < nchunks) issue_qk(c + 1);
 
         // Gram readout. Quarter q: rows 32(q&1).. of A (q < 2) or P (q >= 2);
         // warp u writes output columns [16u, 16u + 16).
@@ -946,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = mma_wait();
         tc_fence_after();
-        if (tid == 0 && c + 1 < nchunks && !v_zero) issue_v(c + 1);
+        if (tid == kTmaThread && c + 1 < nchunks && !v_zero) issue_v(c + 1);
         {  // U^T (D1 columns 16u .. + 16: tokens) -> bf16 A operand of round 4 in TMEM
             float x[16], pk[8];
             tmem_ld16(tq + TM_D1 + 16 * u, x);
