@@ -51,6 +51,49 @@ def test_commit_accepted_prefix(io):
         assert_s(S[sl], h_ref, inputs.io_dtype(io), f"state after {m} accepted tokens")
 
 
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_long_draft_crosses_token_blocks(io):
+    """K = 19 drafts (more than one block of eight): verify outputs for all of
+    them, and commits of accepted prefixes that end inside, at and past a
+    block boundary."""
+    N, K, H, d = 6, 19, 2, 128
+    x = draft(N, K, H, d, io, 27)
+    S = x["h0"].clone()
+    o = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S)
+    torch.cuda.synchronize()
+    assert torch.equal(S, x["h0"])
+    xc = {n: t.cpu() for n, t in x.items()}
+    o_ref, _ = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, inputs.io_dtype(io))
+    acc = [7, 8, 9, 16, 17, 19]
+    ntok = torch.tensor(acc, dtype=torch.int32, device=DEV)
+    kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, ntok=ntok, commit=True,
+                         want_o=False)
+    torch.cuda.synchronize()
+    for n, m in enumerate(acc):
+        sl = slice(n, n + 1)
+        _, h_ref = oracle.prefill(xc["q"][sl, :m], xc["k"][sl, :m], xc["v"][sl, :m],
+                                  xc["g"][sl, :m], xc["beta"][sl, :m], xc["h0"][sl])
+        assert_s(S[sl], h_ref, inputs.io_dtype(io), f"state after {m} accepted tokens")
+
+
+def test_decay_at_its_bound_over_long_drafts():
+    """g = -5 everywhere (the strongest decay allowed) over 16 drafts."""
+    N, K, H, d = 3, 16, 2, 128
+    x = draft(N, K, H, d, "f32", 28)
+    x["g"].fill_(-5.0)
+    S = x["h0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, commit=True,
+                             status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    xc = {n: t.cpu() for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, torch.float32)
+    assert_s(S, h_ref, torch.float32)
+
+
 def test_commit_all_equals_single_steps():
     N, K, H, d = 4, 4, 3, 128
     x = draft(N, K, H, d, "bf16", 23)
