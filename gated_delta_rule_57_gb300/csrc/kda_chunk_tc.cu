@@ -28,25 +28,29 @@
 //   round 3  D1[:, 0:64] = V^T T'^T + (-Y^T) T'^T -> U^T        (A = the v tile, MN-major; -Y^T)
 //   round 4  S^T += U^T Kb                 (S^T pre-scaled by e^{G_C} per key channel)
 //            D1[:, 64:128] += U^T P^T      -> O^T = (Qt S0 + P U)^T   (A = U^T in TMEM)
-// O^T is read out (a warp store covers 32 value channels of one token) while
-// the next chunk's round 1 runs.
+// O^T is read out while the next chunk's round 1 runs, staged in shared
+// memory as bf16 rows and written to o by one TMA store.
 //
 // Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
 // lane quarter), ~220 KB of shared memory (one CTA per SM), 480 TMEM columns:
 // the fp32 state stays in tensor memory for the whole sequence. Inputs arrive
 // by TMA with the 128-byte swizzle (q, k, v in the layout the MMA descriptors
 // expect; g in 32-channel blocks); the next chunk's g, q/k, v and beta are
-// prefetched as soon as their buffers are free. Thread 0 issues rounds 1, 3
-// and 4, a thread of warp 15 round 2; completion is signalled through
-// mbarriers whose waits are bounded (timeout -> KDA_DEV_TIMEOUT). A CTA
-// barrier stands only where a phase reads other warps' results. The decay
-// scan, the decay constants and the operand build need none: each warp owns
-// eight channels of all four tiles, so tile totals and constants stay inside
-// the warp, and it stores its Kt, Qt and Kb rows as it builds them. Round 1
-// waits on an arrive-only mbarrier. Intermediates never leave the SM: the
-// kernel reads each input once and writes o (and hT) once. The <true>
-// instantiation also runs the passes of the time-segmented evaluation and of
-// a sequence split across devices (see TcParams).
+// prefetched as soon as their buffers are free. Issuing a tcgen05.mma keeps
+// the issuing thread busy for about the product's duration, so rounds 1, 2
+// and 4 and the O store are issued by a thread of warp 15, whose own results
+// (P rows, a share of -Y) are needed only later in the chunk; thread 0
+// issues round 3. Completion is signalled through mbarriers whose waits are
+// bounded (timeout -> KDA_DEV_TIMEOUT). A CTA barrier stands only where a
+// phase reads other warps' results. The decay scan, the decay constants and
+// the operand build need none: each warp owns eight channels of all four
+// tiles (a lane scans one channel of one tile in registers), so tile totals
+// and constants stay inside the warp, and it stores its Kt, Qt and Kb rows
+// as it builds them. Round 1 waits on an arrive-only mbarrier.
+// Intermediates never leave the SM: the kernel reads each input once and
+// writes o (and hT) once. The <true> instantiation also runs the passes of
+// the time-segmented evaluation and of a sequence split across devices (see
+// TcParams).
 #include <cudaTypedefs.h>
 
 #include "kda_internal.cuh"
@@ -60,9 +64,10 @@ using namespace ptx;
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
 constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
-// Round 2 is issued by warp 15, which has no other work during the solve
-// (issuing keeps a thread busy for about the MMA's duration).
-constexpr int kRound2Thread = kThreads - 32;
+// Rounds 1, 2 and 4 and the O store are issued by warp 15 (issuing keeps a
+// thread busy for about the MMA's duration; warp 15's other results are
+// needed only late in the chunk).
+constexpr int kIssueThread = kThreads - 32;
 // The next chunk's q/k and v tiles are requested by warp 10, idle in the solve.
 constexpr int kTmaThread = 320;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -77,7 +82,9 @@ constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major B of 
 constexpr uint32_t OFF_KB = 139264;    // Kb of even chunks, SW128 64 x 128 (MN-major B)
 constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major B of round 2)
 constexpr uint32_t OFF_KB1 = 188416;   // Kb of odd chunks
+constexpr uint32_t OFF_OST = 204800;   // O rows of a chunk, bf16 [64][128] (TMA store source)
 constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
+static_assert(OFF_OST + 64 * 256 <= OFF_BETA, "O staging overlaps beta");
 constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
 constexpr uint32_t SMEM_BYTES = 221952 + 1024;
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
@@ -193,6 +200,42 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
         "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
         : "memory");
+}
+// 16 columns at ta and 32 at tb (32x32b) under a single wait.
+__device__ __forceinline__ void tmem_ld16_32(uint32_t ta, uint32_t tb, float* va, float* vb) {
+    uint32_t r[48];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%48];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%49];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) va[i] = __uint_as_float(r[i]);
+#pragma unroll
+    for (int i = 0; i < 32; i++) vb[i] = __uint_as_float(r[16 + i]);
+}
+// Shared -> global tiled bulk copy (4-D map), tracked as a bulk group.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1,
+                                             int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n\t"
+        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Two bf16 (a in the low half) as the fp32 bit pattern tcgen05.st takes.
 __device__ __forceinline__ float pack2f(float a, float b) { return __uint_as_float(pack_bf16(a, b)); }
@@ -359,7 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
-                        const __grid_constant__ CUtensorMap map_g, const TcParams p) {
+                        const __grid_constant__ CUtensorMap map_g,
+                        const __grid_constant__ CUtensorMap map_o, const TcParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // Align to 1024 bytes (the 128-byte swizzle atom) by offsetting the
     // __shared__ array itself, so every access below stays an LDS/STS: an
@@ -486,6 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) =
             0u;
     }
+    // Likewise P's upper right 32 x 32 block (rows 0..31, columns 32..63).
+    for (int e = tid; e < 32 * 16; e += kThreads)
+        *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(64 + (e >> 4), 32 + 2 * (e & 15), 128)) = 0u;
     // Incoming state -> TMEM, transposed: lane j = value channel j, column i
     // = key channel i (a warp reads 128 contiguous bytes of a state row per load).
     {
@@ -506,16 +553,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O of chunk cc -> global: O^T sits in D1 columns 64 + r (token r), lane j
     // (value channel j); warp column group u takes tokens [16u, 16u + 16), so a
     // warp store covers 32 consecutive value channels of one token.
-    auto store_o = [&](int cc, int len) {
-        if (kind == 1) return;
-        float x[16];
-        tmem_ld16(tq + TM_D1 + 64 + 16 * u, x);
+    auto write_o = [&](int cc, int len, const float* x) {
         // A NaN or Inf in q, k or v reaches some output through the
         // recurrence; x * 0 is 0 for finite x and NaN otherwise.
         float pr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 16; e++) pr[e & 3] = fmaf(x[e], 0.f, pr[e & 3]);
         if ((pr[0] + pr[1]) + (pr[2] + pr[3]) != 0.f) flags |= KDA_DEV_NONFINITE;
+        if (kind == 0) {  // staged: one TMA store writes the chunk's rows (rows past T are clipped)
+            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OST) + 16 * u * kD + lane;
+#pragma unroll
+            for (int e = 0; e < 16; e++) st[e * kD] = __float2bfloat16_rn(x[e]);
+            return;
+        }
         __nv_bfloat16* dst = p.o + (((size_t)b * T + t_begin + cc * kC) * p.H + h) * kD + lane;
         const size_t rs = (size_t)p.H * kD;
 #pragma unroll
@@ -527,6 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dst[r * rs] = __float2bfloat16_rn(val);
             }
         }
+    };
+    auto store_o = [&](int cc, int len) {
+        if (kind == 1) return;
+        float x[16];
+        tmem_ld16(tq + TM_D1 + 64 + 16 * u, x);
+        write_o(cc, len, x);
     };
 
     uint32_t mma_phase = 0;
@@ -579,85 +635,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sbeta[tid] = beta_next;
             }
             beta_next = load_beta(c + 1);
+            float cv6[5];
+            // Decay scan, one column per lane: lane (a, j) takes channel c0 + j
+            // of tile a, its 16 rows in the order 2a, 2a + 1, .. (mod 16), so the
+            // rows one load touches lie in four different swizzle classes.
+            // Rows i and i + 8 of the order share a class and differ in byte
+            // offset by 1024.
+            {
+                const uint32_t cb = gch + (uint32_t)(j >> 2), w4 = 4u * (uint32_t)(j & 3);
+                uint32_t off[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const uint32_t rr = (uint32_t)((i + 2 * a) & 15);
+                    off[i] = (uint32_t)(16 * a + rr) * 128u + ((cb ^ (rr & 7u)) << 4) + w4;
+                }
+                float sc[16];  // inclusive sums along the rotated order, log2 units
+                float mn = 0.f, mx = -5.f, run = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const float x = *reinterpret_cast<const float*>(gblk + (off[i & 7] ^ (i >= 8 ? 1024u : 0u)));
+                    mn = fminf(mn, x);
+                    mx = fmaxf(mx, x);
+                    run = fmaf(x, kLog2e, run);
+                    sc[i] = run;
+                }
+                const float tot = sc[15];
+                if (!(fabsf(tot) <= 3.402823466e38f)) flags |= KDA_DEV_NONFINITE;
+                else if (mn < kLogDecayMin || mx > 0.f) flags |= KDA_DEV_DECAY_RANGE;
+                // rows 2a .. 15 come first in the order: natural prefix =
+                // sc + (rows 0 .. 2a - 1) there, sc - (rows 2a .. 15) after the wrap
+                const float tail = a == 0 ? sc[15] : a == 1 ? sc[13] : a == 2 ? sc[11] : sc[9];
+                const float head = tot - tail;
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const float pv = (2 * a <= 15 - i) ? sc[i] + head : sc[i] - tail;
+                    *reinterpret_cast<float*>(gblk + (off[i & 7] ^ (i >= 8 ? 1024u : 0u))) = pv;
+                }
+                // Per (tile, channel) decay constants of tile a, channel c0 + j:
+                //   0: e^{G_a-}  1: e^{G_C - G_a+}  2: e^{tile total}  4, 5: e^{G_{a'-} - G_a+}, a' = 2, 3
+                // (a' = 1 would be e^0 for tile 0: not stored)
+                float tb[4];
+#pragma unroll
+                for (int bb = 0; bb < 4; bb++) tb[bb] = __shfl_sync(0xffffffffu, tot, 8 * bb + j);
+                float pre = 0.f, post = 0.f;
+#pragma unroll
+                for (int bb = 0; bb < 4; bb++) {
+                    if (bb < a) pre += tb[bb];
+                    if (bb > a) post += tb[bb];
+                }
+                cv6[0] = fast_exp2(pre);
+                cv6[1] = fast_exp2(post);
+                cv6[2] = fast_exp2(tot);
+                cv6[3] = fast_exp2(a < 1 ? tb[1] : 0.f);
+                cv6[4] = fast_exp2((a < 1 ? tb[1] : 0.f) + (a < 2 ? tb[2] : 0.f));
+                if (a == 0) slam[c0 + j] = fast_exp2(tb[0] + tb[1] + tb[2] + tb[3]);
+            }
+            __syncwarp();  // the column prefixes are in the g buffer
             float gam[2][8];  // in-tile inclusive cumulative log2-decay, rows j and j + 8
-            float mn = 0.f, mx = -5.f, sum = 0.f;
 #pragma unroll
             for (int e = 0; e < 2; e++) {
                 const int r = 16 * a + j + 8 * e;
 #pragma unroll
                 for (int hq = 0; hq < 2; hq++) {
                     const float4 v = *reinterpret_cast<const float4*>(grow_chunk(r, hq));
-                    const float gv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int z = 0; z < 4; z++) {
-                        mn = fminf(mn, gv[z]);
-                        mx = fmaxf(mx, gv[z]);
-                        sum += gv[z];
-                        gam[e][4 * hq + z] = gv[z] * kLog2e;
-                    }
+                    gam[e][4 * hq] = v.x; gam[e][4 * hq + 1] = v.y;
+                    gam[e][4 * hq + 2] = v.z; gam[e][4 * hq + 3] = v.w;
                 }
             }
-            if (!(fabsf(sum) <= 3.402823466e38f)) flags |= KDA_DEV_NONFINITE;
-            else if (mn < kLogDecayMin || mx > 0.f) flags |= KDA_DEV_DECAY_RANGE;
-            // Inclusive scans over the 8 lanes of the tile: rows j (e = 0) and
-            // j + 8 (e = 1, offset by the first half's total from lane j = 7).
+            __syncwarp();  // every lane has its prefixes: rows 0 .. 19 take the constants
 #pragma unroll
-            for (int z = 0; z < 8; z++) {
-                float x0 = gam[0][z], x1 = gam[1][z];
-#pragma unroll
-                for (int off = 1; off < 8; off <<= 1) {
-                    const float y0 = __shfl_up_sync(0xffffffffu, x0, off, 8);
-                    const float y1 = __shfl_up_sync(0xffffffffu, x1, off, 8);
-                    if (j >= off) { x0 += y0; x1 += y1; }
-                }
-                gam[0][z] = x0;
-                gam[1][z] = x1 + __shfl_sync(0xffffffffu, x0, 7, 8);
-            }
-            __syncwarp();  // every lane has read its g values
-            // tile totals (lane j = 7 holds them in row j + 8 = 15) -> row 24 + a
-            if (j == 7) {
-                *reinterpret_cast<float4*>(grow_chunk(24 + a, 0)) =
-                    make_float4(gam[1][0], gam[1][1], gam[1][2], gam[1][3]);
-                *reinterpret_cast<float4*>(grow_chunk(24 + a, 1)) =
-                    make_float4(gam[1][4], gam[1][5], gam[1][6], gam[1][7]);
-            }
-            __syncwarp();
-            // Per (tile, channel) decay constants; lane (a, j) computes those
-            // of tile a, channel c0 + j, into row 6a + k6:
-            //   0: e^{G_a-}  1: e^{G_C - G_a+}  2: e^{tile total}  3..5: e^{G_{a'-} - G_a+}, a' = 1..3
-            {
-                float tb[4];
-#pragma unroll
-                for (int bb = 0; bb < 4; bb++)
-                    tb[bb] = reinterpret_cast<const float*>(grow_chunk(24 + bb, j >> 2))[j & 3];
-                float pre = 0.f, post = 0.f, own = 0.f;
-#pragma unroll
-                for (int bb = 0; bb < 4; bb++) {
-                    if (bb < a) pre += tb[bb];
-                    if (bb > a) post += tb[bb];
-                    if (bb == a) own = tb[bb];
-                }
-                float cv[6];
-                cv[0] = fast_exp2(pre);
-                cv[1] = fast_exp2(post);
-                cv[2] = fast_exp2(own);
-                float run = 0.f;
-#pragma unroll
-                for (int ap = 1; ap < 4; ap++) {
-                    cv[2 + ap] = fast_exp2(run);
-                    if (ap > a) run += tb[ap];
-                }
-                if (a == 0) slam[c0 + j] = fast_exp2(tb[0] + tb[1] + tb[2] + tb[3]);
-#pragma unroll
-                for (int k6 = 0; k6 < 6; k6++)
-                    reinterpret_cast<float*>(grow_chunk(6 * a + k6, j >> 2))[j & 3] = cv[k6];
-            }
+            for (int k5 = 0; k5 < 5; k5++)
+                reinterpret_cast<float*>(grow_chunk(5 * a + k5, j >> 2))[j & 3] = cv6[k5];
             __syncwarp();
             float cst[6][8];
 #pragma unroll
             for (int k6 = 0; k6 < 6; k6++) {
-                const float4 w0 = *reinterpret_cast<const float4*>(grow_chunk(6 * a + k6, 0));
-                const float4 w1 = *reinterpret_cast<const float4*>(grow_chunk(6 * a + k6, 1));
+                if (k6 == 3) {
+#pragma unroll
+                    for (int z = 0; z < 8; z++) cst[3][z] = 1.f;
+                    continue;
+                }
+                const int k5 = k6 < 3 ? k6 : k6 - 1;
+                const float4 w0 = *reinterpret_cast<const float4*>(grow_chunk(5 * a + k5, 0));
+                const float4 w1 = *reinterpret_cast<const float4*>(grow_chunk(5 * a + k5, 1));
                 cst[k6][0] = w0.x; cst[k6][1] = w0.y; cst[k6][2] = w0.z; cst[k6][3] = w0.w;
                 cst[k6][4] = w1.x; cst[k6][5] = w1.y; cst[k6][6] = w1.z; cst[k6][7] = w1.w;
             }
@@ -718,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[BAR_P1]);
 
         // ------------------------------------------------------------ round 1: Gram
-        if (tid == 0) {
+        if (tid == kIssueThread) {
             if (!mbar_wait(&bars[BAR_P1], par)) flags |= KDA_DEV_TIMEOUT;
             tc_fence_after();
             // The four windows are consecutive rows of one tile, so a single
@@ -738,13 +798,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // only ever set by a failed wait, so it fails the vote after the readout.)
         ok = r4_wait() && !(flags & KDA_DEV_TIMEOUT);
         if (!ok) flags |= KDA_DEV_TIMEOUT;
-        // The previous (full) chunk's O rows, D1 lanes 64..127 -> global.
-        if (c > 0 && ok) store_o(c - 1, kC);
+        // The O staging buffer: the previous chunk's store has read it (its
+        // issuer arrived on BAR_P1 after waiting for that).
+        if (kind == 0 && !mbar_wait(&bars[BAR_P1], par)) flags |= KDA_DEV_TIMEOUT;
         if (ok) {
+            // The previous (full) chunk's O rows (D1 columns 64..127) -> global;
             // S0^T (lane = value channel, columns = key channels 32u ..) -> bf16
             // A operand of round 2 in TMEM; S <- e^{G_C} S (per key channel).
             float y[32];
-            tmem_ld32(tq + TM_S + 32 * u, y);
+            if (c > 0 && kind != 1) {
+                float xo[16];
+                tmem_ld16_32(tq + TM_D1 + 64 + 16 * u, tq + TM_S + 32 * u, xo, y);
+                write_o(c - 1, kC, xo);
+            } else {
+                tmem_ld32(tq + TM_S + 32 * u, y);
+            }
             if (SEG && v_zero) {
                 bool nz = false;
 #pragma unroll
@@ -780,43 +848,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == kTmaThread && c + 1 < nchunks) issue_qk(c + 1);
 
         // Gram readout. Quarter q: rows 32(q&1).. of A (q < 2) or P (q >= 2);
-        // warp u writes output columns [16u, 16u + 16).
+        // warp u writes output columns [16u, 16u + 16). Only blocks that are
+        // read are written: the solve reads A strictly below the diagonal (its
+        // diagonal blocks' upper parts are loaded but never used), and P's
+        // blocks right of the diagonal are zero (the upper right 32 x 32 block
+        // is cleared once; warps u > a0 + 1 have nothing to write).
         {
             const int part = q >> 1;
             const int r = 32 * (q & 1) + (tid & 31);
             const int a = r >> 4, a0 = 2 * (q & 1);
-            float v0[16], v1[16];
+            if (u <= a0 + 1) {
+                float v0[16], v1[16];
+                if (u <= a0) {
+                    tmem_ld16x2(tq + TM_SCR + win_row(a0) + 16 * u, tq + TM_SCR + win_row(a0 + 1) + 16 * u,
+                                v0, v1);
+                } else {
+                    tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * u, v1);
 #pragma unroll
-            for (int jj = 0; jj < 16; jj++) { v0[jj] = 0.f; v1[jj] = 0.f; }
-            if (u <= a0)
-                tmem_ld16x2(tq + TM_SCR + win_row(a0) + 16 * u, tq + TM_SCR + win_row(a0 + 1) + 16 * u,
-                            v0, v1);
-            else if (u == a0 + 1)
-                tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * u, v1);
-            const bool second = (a == a0 + 1);
-            const bool live = (u <= a);
-            float out[16];
-            if (part == 0) {
-                const float br = sbeta[r];
-#pragma unroll
-                for (int jj = 0; jj < 16; jj++) {
-                    const int s = 16 * u + jj;
-                    const float val = second ? v1[jj] : v0[jj];
-                    out[jj] = (live && s < r) ? br * val : 0.f;
+                    for (int jj = 0; jj < 16; jj++) v0[jj] = v1[jj];  // rows of tile a0: not read
                 }
-                float4* FA = reinterpret_cast<float4*>(sm + OFF_FA + (r * LDA + 16 * u) * 4);
+                const bool second = (a == a0 + 1);
+                float out[16];
+                if (part == 0) {
+                    const float br = sbeta[r];
 #pragma unroll
-                for (int jj = 0; jj < 4; jj++)
-                    FA[jj] = make_float4(out[4 * jj], out[4 * jj + 1], out[4 * jj + 2], out[4 * jj + 3]);
-            } else {
+                    for (int jj = 0; jj < 16; jj++) out[jj] = br * (second ? v1[jj] : v0[jj]);
+                    float4* FA = reinterpret_cast<float4*>(sm + OFF_FA + (r * LDA + 16 * u) * 4);
 #pragma unroll
-                for (int jj = 0; jj < 16; jj++) {
-                    const int s = 16 * u + jj;
-                    const float val = second ? v1[jj] : v0[jj];
-                    out[jj] = (live && s <= r) ? val : 0.f;
+                    for (int jj = 0; jj < 4; jj++)
+                        FA[jj] = make_float4(out[4 * jj], out[4 * jj + 1], out[4 * jj + 2], out[4 * jj + 3]);
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj++) {
+                        const int s = 16 * u + jj;
+                        const float val = second ? v1[jj] : v0[jj];
+                        out[jj] = (u < a || (u == a && s <= r)) ? val : 0.f;
+                    }
+                    st_row8(sm + OFF_A0, 64 + r, 16 * u, 128, out);
+                    st_row8(sm + OFF_A0, 64 + r, 16 * u + 8, 128, out + 8);
                 }
-                st_row8(sm + OFF_A0, 64 + r, 16 * u, 128, out);
-                st_row8(sm + OFF_A0, 64 + r, 16 * u + 8, 128, out + 8);
             }
         }
         tc_fence_before();
@@ -849,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
             unsigned char* TP = sm + OFF_A0;  // T' rows 0..63
-            if (tid == kRound2Thread) {
+            if (tid == kIssueThread) {
                 // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
                 if (!mbar_wait(&bars[BAR_GP], par)) flags |= KDA_DEV_TIMEOUT;
                 tc_fence_after();
@@ -861,6 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, bd0 + kstep_kmajor(128, kk),
                                 idesc, kk > 0);
                 mma_commit(&bars[BAR_R2]);
+                if (c > 0 && kind == 0) {
+                    tma_store_4d(&map_o, sm + OFF_OST, 0, h, t_begin + (c - 1) * kC, b);
+                    bulk_wait_read();
+                }
             }
             if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
                 const int o0 = 16 * warp, jc = tid & 15;
@@ -962,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__syncthreads_or(!ok)) { failed = true; break; }
 
         // ------------------------------------------------------------ round 4: S += Kb^T U, O += P U
-        if (tid == 0) {
+        if (tid == kIssueThread) {
             tc_fence_after();
             // S^T += U^T Kb (B = Kb, MN-major), O^T += U^T P^T (B = P, K-major); A = U^T in TMEM
             const uint32_t idesc = idesc_bf16(128, 128, 0, 1);
@@ -1000,8 +1074,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed && r4_pending && __syncthreads_or(!r4_wait())) failed = true;
     if (failed) flags |= KDA_DEV_TIMEOUT;
     // O rows of the last chunk.
-    if (nchunks > 0 && !failed && !zero_exit)
+    if (nchunks > 0 && !failed && !zero_exit) {
         store_o(nchunks - 1, min(kC, T - t_begin - (nchunks - 1) * kC));
+        if (kind == 0) {
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tma_store_4d(&map_o, sm + OFF_OST, 0, h, t_begin + (nchunks - 1) * kC, b);
+                bulk_wait_all();
+            }
+        }
+    }
+    if (tid == kIssueThread) bulk_wait_all();
     // Final state -> hT.
     // Final state: hT (whole sequences), the segment's zero-start state or
     // its transition (segment pass), nothing (correction pass).
@@ -1048,7 +1132,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 4-D map over [B, T, H, d] (innermost first: d, H, T, B), boxes of
 // box_inner x 1 x 64 x 1 with the 128-byte swizzle. Rows past T read as zero.
 bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, int B, int T,
-              int H, int d, int box_inner) {
+              int H, int d, int box_inner,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -1057,7 +1142,7 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, 
     cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, (cuuint32_t)kC, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1066,7 +1151,7 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz, 
 namespace {
 
 struct TcMaps {
-    CUtensorMap q{}, k{}, v{}, g{};
+    CUtensorMap q{}, k{}, v{}, g{}, o{};
 };
 
 bool make_maps(TcMaps* m, const ChunkFwdArgs& a) {
@@ -1074,7 +1159,9 @@ bool make_maps(TcMaps* m, const ChunkFwdArgs& a) {
     return make_map(&m->q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
            make_map(&m->k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
            make_map(&m->v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
-           make_map(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.H, kD, 32);
+           make_map(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.H, kD, 32) &&
+           (!a.o || make_map(&m->o, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, kD,
+                             CU_TENSOR_MAP_SWIZZLE_NONE));
 }
 
 TcParams base_params(const ChunkFwdArgs& a) {
@@ -1095,7 +1182,8 @@ cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaSt
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel<SEG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kda_chunk_tc_kernel<SEG><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.g, p);
+    kda_chunk_tc_kernel<SEG><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.g, m.o,
+                                                                                 p);
     return cudaGetLastError();
 }
 
