@@ -68,6 +68,9 @@ constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
 // thread busy for about the MMA's duration; warp 15's other results are
 // needed only late in the chunk).
 constexpr int kIssueThread = kThreads - 32;
+// Round 2, the O store and the next g load: warp 12, which has no readout
+// rows and waits for round 2 itself.
+constexpr int kR2Thread = 384;
 // The next chunk's q/k and v tiles are requested by warp 10, idle in the solve.
 constexpr int kTmaThread = 320;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -899,6 +902,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp < 8) named_sync(3, 384);
             else if (q < 2) asm volatile("bar.arrive 3, 384;" ::: "memory");
         }
+        if (!SEG || !(v_zero && s_nz[par] == 0)) {
+            if (tid == kR2Thread) {
+                // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
+                if (!mbar_wait(&bars[BAR_GP], par)) flags |= KDA_DEV_TIMEOUT;
+                tc_fence_after();
+                // D1^T: [Y^T | (Qt S0)^T] = S0^T [Kt; Qt]^T, A = S0^T in TMEM.
+                const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+                const uint64_t bd0 = desc_kmajor(sbase + OFF_AKQ);
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++)
+                    mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, bd0 + kstep_kmajor(128, kk),
+                                idesc, kk > 0);
+                mma_commit(&bars[BAR_R2]);
+                if (c > 0 && kind == 0) {
+                    tma_store_4d(&map_o, sm + OFF_OST, 0, h, t_begin + (c - 1) * kC, b);
+                    bulk_wait_read();
+                }
+            }
+        }
         if (SEG && v_zero && s_nz[par] == 0) {
             // With v = 0 and an incoming state that is exactly zero in fp32,
             // every later state and output of the run is exactly zero: the
@@ -919,23 +941,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* FT = reinterpret_cast<float*>(sm + OFF_FT);
             float* MS = reinterpret_cast<float*>(sm + OFF_MS);
             unsigned char* TP = sm + OFF_A0;  // T' rows 0..63
-            if (tid == kIssueThread) {
-                // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
-                if (!mbar_wait(&bars[BAR_GP], par)) flags |= KDA_DEV_TIMEOUT;
-                tc_fence_after();
-                // D1^T: [Y^T | (Qt S0)^T] = S0^T [Kt; Qt]^T, A = S0^T in TMEM.
-                const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
-                const uint64_t bd0 = desc_kmajor(sbase + OFF_AKQ);
-#pragma unroll
-                for (int kk = 0; kk < 8; kk++)
-                    mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, bd0 + kstep_kmajor(128, kk),
-                                idesc, kk > 0);
-                mma_commit(&bars[BAR_R2]);
-                if (c > 0 && kind == 0) {
-                    tma_store_4d(&map_o, sm + OFF_OST, 0, h, t_begin + (c - 1) * kC, b);
-                    bulk_wait_read();
-                }
-            }
             if (warp < 4) {  // diagonal 16x16 blocks: warp = block, lane j = column j
                 const int o0 = 16 * warp, jc = tid & 15;
                 float acc[16], x[16];
@@ -1085,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (tid == kIssueThread) bulk_wait_all();
+    if (tid == kR2Thread) bulk_wait_all();
     // Final state -> hT.
     // Final state: hT (whole sequences), the segment's zero-start state or
     // its transition (segment pass), nothing (correction pass).
