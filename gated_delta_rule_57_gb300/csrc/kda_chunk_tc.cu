@@ -893,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         tc_fence_before();
-        if (SEG) {  // the segment passes decide on an early stop here: a CTA barrier
+        if (SEG && v_zero) {  // runs with v = 0 decide on an early stop here: a CTA barrier
             if (__syncthreads_or(!ok)) { failed = true; break; }
         } else {
             if (!ok) flags |= KDA_DEV_TIMEOUT;  // voted on at the end of the solve
