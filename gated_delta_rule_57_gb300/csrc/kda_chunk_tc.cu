@@ -20,12 +20,14 @@
 // Since W S0 = T' (Kt S0), the state enters only through Y = Kt S0 and
 // Qt S0, which need neither the Gram matrices nor the solve. The state is kept
 // transposed in tensor memory (lane = value channel j, column = key channel
-// i), so its bf16 copy, -Y and U serve as A operands straight from TMEM (two
-// bf16 per 32-bit column). As 128-row MMAs (D^T = A B^T):
+// i), so its bf16 copy, V - Y and U serve as A operands straight from TMEM
+// (two bf16 per 32-bit column). As 128-row MMAs (D^T = A B^T):
 //   round 1  Gram blocks  [Kp; Qp] * [Km_0; Km_1; Km_2; Km_3]^T   (N = 16+32+48+64)
-//   round 2  D1 = S0^T [Kt; Qt]^T          -> [Y^T | (Qt S0)^T]  (A = S0^T in TMEM; under the solve)
-//            -Y^T -> bf16 A operand in TMEM (under the solve as well)
-//   round 3  D1[:, 0:64] = V^T T'^T + (-Y^T) T'^T -> U^T        (A = the v tile, MN-major; -Y^T)
+//   round 2  D1[:, 0:64] = V^T I (A = the v tile, MN-major; I a constant
+//            identity), then D1 += S0^T [-Kt; Qt]^T -> [(V - Y)^T | (Qt S0)^T]
+//            (A = S0^T in TMEM; under the solve)
+//            (V - Y)^T -> bf16 A operand in TMEM (under the solve as well)
+//   round 3  D1[:, 0:64] = (V - Y)^T T'^T -> U^T                  (A = (V - Y)^T in TMEM)
 //   round 4  S^T += U^T Kb                 (S^T pre-scaled by e^{G_C} per key channel)
 //            D1[:, 64:128] += U^T P^T      -> O^T = (Qt S0 + P U)^T   (A = U^T in TMEM)
 // O^T is read out while the next chunk's round 1 runs, staged in shared
@@ -80,7 +82,7 @@ constexpr uint32_t OFF_G = 0;          // g: 4 blocks of 32 channels, SW128; the
                                        // decay constants (each warp in its own 8 channels' chunks)
 constexpr uint32_t OFF_KQP = 32768;    // [k; q] -> [Kp; Qp], SW128, 128 rows x 128
 constexpr uint32_t OFF_KM = 65536;     // Km windows (160 rows x 128) | solve scratch
-constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major A of round 3)
+constexpr uint32_t OFF_V = 106496;     // v, SW128, 64 rows x 128 (MN-major A of the V^T copy)
 constexpr uint32_t OFF_A0 = 122880;    // [T'; P], SW128 128 x 64 (K-major B of rounds 3, 4)
 constexpr uint32_t OFF_KB = 139264;    // Kb of even chunks, SW128 64 x 128 (MN-major B)
 constexpr uint32_t OFF_AKQ = 155648;   // [Kt; Qt], SW128 128 x 128 (K-major B of round 2)
@@ -89,7 +91,9 @@ constexpr uint32_t OFF_OST = 204800;   // O rows of a chunk, bf16 [64][128] (TMA
 constexpr uint32_t OFF_BETA = 221184;  // fp32 [64]
 static_assert(OFF_OST + 64 * 256 <= OFF_BETA, "O staging overlaps beta");
 constexpr uint32_t OFF_LAM = 221440;   // fp32 [128]  e^{G_C}
-constexpr uint32_t SMEM_BYTES = 221952 + 1024;
+constexpr uint32_t OFF_I = 222208;     // identity 64 x 64 bf16, SW128 K-major (B of the V^T copy)
+static_assert(OFF_I % 1024 == 0 && OFF_I >= OFF_LAM + 512, "identity tile misplaced");
+constexpr uint32_t SMEM_BYTES = OFF_I + 8192 + 1024;
 // aliases inside OFF_KM (solve scratch lives between round 1 and the end of
 // the solve)
 constexpr int LDA = 68;  // fp32 A: TF32 fragment loads (bank 4g + t) and float4 row stores conflict-free
@@ -104,8 +108,8 @@ static_assert(LDA % 4 == 0 && LDT % 4 == 0 && OFF_FA % 16 == 0 && OFF_FT % 16 ==
               "ldmatrix rows must start on 16-byte boundaries");
 
 // TMEM columns: the transposed state, round 2/3/4 accumulators (D1), the
-// Gram round's accumulator (SCR), and bf16 A operands (AUX: S0^T, then -Y^T
-// in columns 0..31 and U^T in 32..63).
+// Gram round's accumulator (SCR), and bf16 A operands (AUX: S0^T, then
+// (V - Y)^T in columns 0..31 and U^T in 32..63).
 constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_SCR = 256, TM_AUX = 416, TM_COLS = 512;
 
 enum { BAR_QK = 0, BAR_G = 1, BAR_V = 2, BAR_MMA = 3, BAR_R4 = 4, BAR_R2 = 5, BAR_P1 = 6, BAR_GP = 7, NBAR = 8 };
@@ -533,6 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(16 * br + i, 16 * bc + 2 * jp, 128)) =
             0u;
     }
+    // The 64 x 64 identity that copies the v tile into D1 (V^T x I).
+    for (int e = tid; e < 64 * 32; e += kThreads) {
+        const int r = e >> 5, cp = 2 * (e & 31);
+        const uint32_t w = (r == cp ? 0x3F80u : 0u) | (r == cp + 1 ? 0x3F800000u : 0u);
+        *reinterpret_cast<uint32_t*>(sm + OFF_I + sw128_offset(r, cp, 64)) = w;
+    }
     // Likewise P's upper right 32 x 32 block (rows 0..31, columns 32..63).
     for (int e = tid; e < 32 * 16; e += kThreads)
         *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(64 + (e >> 4), 32 + 2 * (e & 15), 128)) = 0u;
@@ -764,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Kb (into this chunk's parity buffer: round 4 of the previous
                 // chunk may still read the other).
 #pragma unroll
-                for (int z = 0; z < 8; z++) t8[z] = kp[z] * cst[0][z];
+                for (int z = 0; z < 8; z++) t8[z] = -(kp[z] * cst[0][z]);  // -Kt: round 2 subtracts Y
                 *reinterpret_cast<uint4*>(sm + OFF_AKQ + 2 * blk * 8192u + ro) = pack8(t8);
 #pragma unroll
                 for (int z = 0; z < 8; z++) t8[z] = qp[z] * cst[0][z];
@@ -815,6 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 write_o(c - 1, kC, xo);
             } else {
                 tmem_ld32(tq + TM_S + 32 * u, y);
+            }
+            {  // round 2 accumulates onto D1: (Qt S0)^T starts from zero
+                float zz[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) zz[e] = 0.f;
+                tmem_st16(tq + TM_D1 + 64 + 16 * u, zz);
             }
             if (SEG && v_zero) {
                 bool nz = false;
@@ -907,13 +923,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Round 2: D1 = [Kt; Qt] S0 = [Y; Qt S0], under the solve.
                 if (!mbar_wait(&bars[BAR_GP], par)) flags |= KDA_DEV_TIMEOUT;
                 tc_fence_after();
-                // D1^T: [Y^T | (Qt S0)^T] = S0^T [Kt; Qt]^T, A = S0^T in TMEM.
+                // D1[:, 0:64] = V^T (V^T x I; A = the v tile, MN-major), then
+                // D1^T += S0^T [-Kt; Qt]^T: [(V - Y)^T | (Qt S0)^T], A = S0^T in TMEM.
+                if (!v_zero) {
+                    if (!mbar_wait(&bars[BAR_V], par)) flags |= KDA_DEV_TIMEOUT;
+                    tc_fence_after();
+                    const uint32_t idesc_v = idesc_bf16(128, 64, 1, 0);
+                    const uint64_t vd0 = desc_mnmajor(sbase + OFF_V, 64);
+                    const uint64_t id0 = desc_kmajor(sbase + OFF_I);
+#pragma unroll
+                    for (int kk = 0; kk < 4; kk++)
+                        mma_bf16(tbase + TM_D1, vd0 + kstep_mnmajor(kk), id0 + kstep_kmajor(64, kk),
+                                 idesc_v, kk > 0);
+                }
                 const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
                 const uint64_t bd0 = desc_kmajor(sbase + OFF_AKQ);
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
                     mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, bd0 + kstep_kmajor(128, kk),
-                                idesc, kk > 0);
+                                idesc, (!v_zero) || kk > 0);
                 mma_commit(&bars[BAR_R2]);
                 if (c > 0 && kind == 0) {
                     tma_store_4d(&map_o, sm + OFF_OST, 0, h, t_begin + (c - 1) * kC, b);
@@ -983,8 +1011,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp < 8) named_sync(2, 256);
             solve_level3(FA, FT, warp, tid & 31, TP, sbeta);
             if (warp >= 8) {
-                // -Y^T (D1 columns 0..63: tokens) -> bf16 A operand of round 3 in
-                // TMEM (AUX columns 0..31; S0^T there is consumed), tokens
+                // (V - Y)^T (D1 columns 0..63: tokens) -> bf16 A operand of round 3
+                // in TMEM (AUX columns 0..31; S0^T there is consumed), tokens
                 // [32 (u - 2), + 32), by the eight warps idle in this level.
                 ok = v_zero || mbar_wait(&bars[BAR_V], par);
                 ok = mbar_wait(&bars[BAR_R2], r2_phase) && ok;
@@ -994,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float y[32], pk[16];
                     tmem_ld32(tq + TM_D1 + t0, y);
 #pragma unroll
-                    for (int e = 0; e < 16; e++) pk[e] = pack2f(-y[2 * e], -y[2 * e + 1]);
+                    for (int e = 0; e < 16; e++) pk[e] = pack2f(y[2 * e], y[2 * e + 1]);
                     tmem_st16(tq + TM_AUX + t0 / 2, pk);
                     tmem_wait_st();
                 }
@@ -1009,20 +1037,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ round 3: U^T = (V - Y)^T T'^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idesc_v = idesc_bf16(128, 64, 1, 0);  // A = v tile (MN-major)
-            const uint32_t idesc_y = idesc_bf16(128, 64, 0, 0);  // A = -Y^T (TMEM)
-            const uint64_t vd0 = desc_mnmajor(sbase + OFF_V, 64);
+            const uint32_t idesc_y = idesc_bf16(128, 64, 0, 0);  // A = (V - Y)^T (TMEM)
             const uint64_t td0 = desc_kmajor(sbase + OFF_A0);    // T': rows 0..63 of [T'; P]
-            if (!v_zero) {
-#pragma unroll
-                for (int kk = 0; kk < 4; kk++)
-                    mma_bf16(tbase + TM_D1, vd0 + kstep_mnmajor(kk), td0 + kstep_kmajor(128, kk),
-                             idesc_v, kk > 0);
-            }
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
                 mma_bf16_ta(tbase + TM_D1, tbase + TM_AUX + 8 * kk, td0 + kstep_kmajor(128, kk),
-                            idesc_y, (!v_zero) || kk > 0);
+                            idesc_y, kk > 0);
             mma_commit(&bars[BAR_MMA]);
         }
         ok = mma_wait();
