@@ -872,17 +872,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // diagonal blocks' upper parts are loaded but never used), and P's
         // blocks right of the diagonal are zero (the upper right 32 x 32 block
         // is cleared once; warps u > a0 + 1 have nothing to write).
-        {
+        auto readout = [&](int ug) {  // column group ug of this warp's lane quarter
             const int part = q >> 1;
             const int r = 32 * (q & 1) + (tid & 31);
             const int a = r >> 4, a0 = 2 * (q & 1);
-            if (u <= a0 + 1) {
+            if (ug <= a0 + 1) {
                 float v0[16], v1[16];
-                if (u <= a0) {
-                    tmem_ld16x2(tq + TM_SCR + win_row(a0) + 16 * u, tq + TM_SCR + win_row(a0 + 1) + 16 * u,
+                if (ug <= a0) {
+                    tmem_ld16x2(tq + TM_SCR + win_row(a0) + 16 * ug, tq + TM_SCR + win_row(a0 + 1) + 16 * ug,
                                 v0, v1);
                 } else {
-                    tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * u, v1);
+                    tmem_ld16(tq + TM_SCR + win_row(a0 + 1) + 16 * ug, v1);
 #pragma unroll
                     for (int jj = 0; jj < 16; jj++) v0[jj] = v1[jj];  // rows of tile a0: not read
                 }
@@ -892,20 +892,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float br = sbeta[r];
 #pragma unroll
                     for (int jj = 0; jj < 16; jj++) out[jj] = br * (second ? v1[jj] : v0[jj]);
-                    float4* FA = reinterpret_cast<float4*>(sm + OFF_FA + (r * LDA + 16 * u) * 4);
+                    float4* FA = reinterpret_cast<float4*>(sm + OFF_FA + (r * LDA + 16 * ug) * 4);
 #pragma unroll
                     for (int jj = 0; jj < 4; jj++)
                         FA[jj] = make_float4(out[4 * jj], out[4 * jj + 1], out[4 * jj + 2], out[4 * jj + 3]);
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 16; jj++) {
-                        const int s = 16 * u + jj;
+                        const int s = 16 * ug + jj;
                         const float val = second ? v1[jj] : v0[jj];
-                        out[jj] = (u < a || (u == a && s <= r)) ? val : 0.f;
+                        out[jj] = (ug < a || (ug == a && s <= r)) ? val : 0.f;
                     }
-                    st_row8(sm + OFF_A0, 64 + r, 16 * u, 128, out);
-                    st_row8(sm + OFF_A0, 64 + r, 16 * u + 8, 128, out + 8);
+                    st_row8(sm + OFF_A0, 64 + r, 16 * ug, 128, out);
+                    st_row8(sm + OFF_A0, 64 + r, 16 * ug + 8, 128, out + 8);
                 }
+            }
+        };
+        // A rows by their own column group; P rows, read only by round 4, by
+        // warps 10, 11, 14, 15 (idle until round 2) so that the solve warps
+        // 2, 3, 6, 7 leave the readout at once.
+        if (q < 2) {
+            readout(u);
+        } else if (u >= 2) {
+            if (q == 2) {
+                readout(u - 2);
+            } else {
+                readout(2 * (u - 2));
+                readout(2 * (u - 2) + 1);
             }
         }
         tc_fence_before();
@@ -913,10 +926,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__syncthreads_or(!ok)) { failed = true; break; }
         } else {
             if (!ok) flags |= KDA_DEV_TIMEOUT;  // voted on at the end of the solve
-            // The solve reads A rows written by warps 0, 1, 4, 5 (synced here), 9,
-            // 13, and its level-3 slabs reuse rows that warps 8, 12 write.
-            if (warp < 8) named_sync(3, 384);
-            else if (q < 2) asm volatile("bar.arrive 3, 384;" ::: "memory");
+            // Each diagonal block's warp waits for the warp that wrote its A rows
+            // (block 0: itself; 1: warp 4; 2: warp 9, which also wrote A_32; 3:
+            // warp 13). A_10 is warp 0's, A_[23][01] that of warps 1 and 5,
+            // which reach the level-3 barrier after writing it.
+            if (warp == 1 || warp == 4) named_sync(5, 64);
+            else if (warp == 2 || warp == 9) named_sync(6, 64);
+            else if (warp == 3 || warp == 13) named_sync(7, 64);
         }
         if (!SEG || !(v_zero && s_nz[par] == 0)) {
             if (tid == kR2Thread) {
