@@ -202,11 +202,15 @@ def time_prefill(x, steps, warmup, world, device):
     w = PREFILL
     o = torch.empty_like(x["v"])
     hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=device)
+    # the prefill's workspace (state handoffs of the balanced schedule), allocated once
+    ws = torch.empty(max(16, kda.kda_chunk_fwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv,
+                                                             x["q"].dtype)),
+                     dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def step():
         kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o=o, hT=hT,
-                          stream=stream)
+                          workspace=ws, stream=stream)
 
     for _ in range(warmup):
         step()

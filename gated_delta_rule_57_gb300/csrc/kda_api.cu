@@ -88,7 +88,11 @@ const char* kda_last_error_string(void) { return g_last_error; }
 size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dtype_t io) {
     if (B < 0 || T < 0 || H < 0) return (size_t)-1;
     if (check_dims(dk, dv, io) != KDA_OK) return (size_t)-1;
-    return 0;  // both prefill paths keep their intermediates on chip
+    if ((long long)B * H >= (1LL << 31)) return (size_t)-1;
+    // The tensor-core path balances sequences over the SMs through a state
+    // handoff buffer; the fp32 path and empty problems need nothing.
+    if (io != KDA_BF16 || dk != 128 || T == 0 || (long long)B * H < 2) return 0;
+    return kda::balanced_workspace_bytes((long long)B * H);
 }
 
 }  // extern "C"
@@ -200,7 +204,8 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
                             int T, int H, int dk, int dv, kda_dtype_t io, float* ckpt,
                             int ckpt_every, int* d_status, void* stream, int nseg = 1,
                             void* workspace = nullptr, size_t ws_bytes = 0,
-                            bool check_only = false) {
+                            bool check_only = false, void* bal_ws = nullptr,
+                            size_t bal_bytes = 0) {
     if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
@@ -276,6 +281,24 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
                         static_cast<cudaStream_t>(stream)};
     a.ckpt = ckpt;
     a.ckpt_every = ckpt ? ckpt_every : 0;
+    // A prefill workspace of the queried size enables the balanced schedule;
+    // without one (or a smaller one) every sequence gets its own CTA.
+    if (bal_ws && nseg_eff <= 1 && io == KDA_BF16 && dk == 128) {
+        const size_t need = kda::balanced_workspace_bytes((long long)B * H);
+        if (bal_bytes < need) {
+            bal_ws = nullptr;
+        } else {
+            if (!aligned16(bal_ws))
+                return fail(KDA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+            const void* all[] = {q, k, v, g, beta, h0, o, hT};
+            const size_t all_bytes[] = {n_qk * esz, n_qk * esz, n_v * esz, n_qk * 4, n_b * 4,
+                                        h0 ? n_s * 4 : 0, n_v * esz, hT ? n_s * 4 : 0};
+            for (int i = 0; i < 8; i++)
+                if (overlaps(bal_ws, need, all[i], all_bytes[i]))
+                    return fail(KDA_ERR_INVALID_ARG, "workspace overlaps another tensor");
+        }
+        a.bal_ws = bal_ws;
+    }
     cudaError_t e = nseg_eff > 1
                         ? kda::launch_chunk_fwd_tc_segmented(a, nseg_eff, seg_chunks, lead,
                                                              static_cast<float*>(workspace))
@@ -297,10 +320,8 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const fl
                            int T, int H, int dk, int dv, kda_dtype_t io, void* workspace,
                            size_t ws_bytes, int* d_status, void* stream) {
     NvtxRange nvtx_range("kda_chunk_fwd");
-    (void)workspace;
-    (void)ws_bytes;
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0,
-                          d_status, stream);
+                          d_status, stream, 1, nullptr, 0, false, workspace, ws_bytes);
 }
 
 kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, const float* g,

@@ -34,8 +34,12 @@
 // memory as bf16 rows and written to o by one TMA store.
 //
 // Execution. One CTA per (b, h) sequence, 512 threads (four warps per TMEM
-// lane quarter), ~220 KB of shared memory (one CTA per SM), 480 TMEM columns:
-// the fp32 state stays in tensor memory for the whole sequence. Inputs arrive
+// lane quarter), ~226 KB of shared memory (one CTA per SM), 480 TMEM columns:
+// the fp32 state stays in tensor memory for the whole sequence. When B * H
+// sequences would leave a partly filled last wave, one CTA per SM instead
+// runs an equal share of chunk steps over the sequences laid end to end (the
+// balanced schedule, see TcParams); a sequence split between two CTAs passes
+// its state through global memory once. Inputs arrive
 // by TMA with the 128-byte swizzle (q, k, v in the layout the MMA descriptors
 // expect; g in 32-channel blocks); the next chunk's g, q/k, v and beta are
 // prefetched as soon as their buffers are free. Issuing a tcgen05.mma keeps
@@ -137,6 +141,14 @@ struct TcParams {
     // v = 0 and writes the slice's transition to ws_m[bh]; pass 4 runs from
     // ws_sin[bh] with v = 0 and adds its outputs to o.
     int pass, nseg, seg_chunks, lead, BH;
+    // Balanced schedule of the whole-sequence kernel (bal_W > 0): CTA i covers
+    // chunk steps [i bal_W, (i + 1) bal_W) of the sequences laid end to end
+    // (bal_W >= the chunks of one sequence); a sequence split between two CTAs
+    // hands its state over through bal_states[bh] and bal_flags[bh] (zeroed
+    // before the launch; all CTAs are resident: cooperative launch).
+    int bal_W;
+    float* bal_states;  // [BH][dk][dv]
+    int* bal_flags;     // [BH]
     float* ws_s0;         // [BH][nseg][dk][dv]
     float* ws_m;          // [BH][nseg - 1][dk][dk]
     const float* ws_sin;  // [BH][nseg - 1][dk][dv]
@@ -243,6 +255,15 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Handoff flag of the balanced schedule (GPU-scope acquire / release).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Two bf16 (a in the low half) as the fp32 bit pattern tcgen05.st takes.
 __device__ __forceinline__ float pack2f(float a, float b) { return __uint_as_float(pack_bf16(a, b)); }
@@ -456,18 +477,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int bh, seg;
     task_seq(&bh, &seg);
-    const int b = bh / p.H, h = bh % p.H;
-    const int t_begin = seg == 0 ? 0 : (p.lead + seg - 1) * p.seg_chunks * kC;
+    int b = bh / p.H, h = bh % p.H;
+    int t_begin = seg == 0 ? 0 : (p.lead + seg - 1) * p.seg_chunks * kC;
     // Initial state: h0 (whole sequences and first segments), zero (other
     // segments), the identity (transition runs) or the incoming state.
     const float* h0p = (kind == 2 && whole) ? p.ws_sin + (size_t)bh * kD * kD
                        : kind == 2 ? p.ws_sin + ((size_t)bh * (p.nseg - 1) + seg - 1) * kD * kD
                        : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * kD * kD
                                                          : nullptr;
-    const int nchunks = whole
-                            ? (T + kC - 1) / kC
-                            : min(seg == 0 ? p.lead * p.seg_chunks : p.seg_chunks,
-                                  (T - t_begin + kC - 1) / kC);
+    int nchunks = whole
+                      ? (T + kC - 1) / kC
+                      : min(seg == 0 ? p.lead * p.seg_chunks : p.seg_chunks,
+                            (T - t_begin + kC - 1) / kC);
+    // Tasks of this CTA: one, except in the balanced schedule, where the range
+    // [lo, hi) of chunk steps gives the head of sequence s_last (chunks
+    // [0, c_last), when c_last < nch), the whole sequences between, and the
+    // tail of sequence s_first (chunks [c_first, nch), when c_first > 0).
+    const bool bal = !SEG && p.bal_W > 0;
+    const int nch = (T + kC - 1) / kC;
+    int ntask = 1, s_first = 0, c_first = 0, s_last = 0, c_last = 0, full_lo = 0;
+    bool has_head = false, has_tail = false;
+    if (bal) {
+        const long long lo = (long long)blockIdx.x * p.bal_W;
+        const long long hi = min(lo + p.bal_W, (long long)p.BH * nch);
+        ntask = 0;
+        if (lo < hi) {
+            s_first = (int)(lo / nch);
+            c_first = (int)(lo % nch);
+            s_last = (int)((hi - 1) / nch);
+            c_last = (int)((hi - 1) % nch) + 1;
+            has_tail = c_first > 0;
+            has_head = c_last < nch;
+            full_lo = has_tail ? s_first + 1 : s_first;
+            const int full_hi = has_head ? s_last - 1 : s_last;
+            ntask = (has_head ? 1 : 0) + max(0, full_hi - full_lo + 1) + (has_tail ? 1 : 0);
+        }
+    }
+    bool from_slot = false, to_slot = false;
+    auto set_task = [&](int ti) {  // balanced schedule: task ti in run order
+        int c0 = 0, c1 = nch;
+        from_slot = to_slot = false;
+        if (has_head && ti == 0) {
+            bh = s_last;
+            c1 = c_last;
+            to_slot = true;
+        } else if (has_tail && ti == ntask - 1) {
+            bh = s_first;
+            c0 = c_first;
+            from_slot = true;
+        } else {
+            bh = full_lo + ti - (has_head ? 1 : 0);
+        }
+        b = bh / p.H;
+        h = bh % p.H;
+        t_begin = c0 * kC;
+        nchunks = c1 - c0;
+        h0p = from_slot ? p.bal_states + (size_t)bh * kD * kD
+              : p.h0    ? p.h0 + (size_t)bh * kD * kD
+                        : nullptr;
+    };
+    if (bal && ntask > 0) set_task(0);
     const uint32_t sbase = smem_addr(sm);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* slam = reinterpret_cast<float*>(sm + OFF_LAM);
@@ -516,17 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sm + OFF_V, &map_v, &bars[BAR_V], 0, h, t_begin + c * kC, b);
         tma_load_4d(sm + OFF_V + 8192, &map_v, &bars[BAR_V], 64, h, t_begin + c * kC, b);
     };
-    if (tid == 0 && nchunks > 0) {
-        issue_qk(0);
-        issue_g(0);
-        if (!v_zero) issue_v(0);
-    }
     // beta is strided by H in memory: plain loads, kept one chunk ahead.
     auto load_beta = [&](int c) {
         const int t = t_begin + c * kC + tid;
         return (tid < kC && c < nchunks && t < T) ? p.beta[((size_t)b * T + t) * p.H + h] : 0.f;
     };
-    float beta_next = load_beta(0);
+    float beta_next = 0.f;
 
     // T' is zero in the six 16 x 16 blocks above the diagonal; nothing else
     // writes there, so they are cleared once.
@@ -546,23 +610,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Likewise P's upper right 32 x 32 block (rows 0..31, columns 32..63).
     for (int e = tid; e < 32 * 16; e += kThreads)
         *reinterpret_cast<uint32_t*>(sm + OFF_A0 + sw128_offset(64 + (e >> 4), 32 + 2 * (e & 15), 128)) = 0u;
-    // Incoming state -> TMEM, transposed: lane j = value channel j, column i
-    // = key channel i (a warp reads 128 contiguous bytes of a state row per load).
-    {
-        float x[32];
-#pragma unroll
-        for (int e = 0; e < 32; e++) {
-            const int i = 32 * u + e;
-            x[e] = kind == 1 ? (lane == i ? 1.f : 0.f) : (h0p ? h0p[(size_t)i * kD + lane] : 0.f);
-        }
-        tmem_st16(tq + TM_S + 32 * u, x);
-        tmem_st16(tq + TM_S + 32 * u + 16, x + 16);
-        tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
     // O of chunk cc -> global: O^T sits in D1 columns 64 + r (token r), lane j
     // (value channel j); warp column group u takes tokens [16u, 16u + 16), so a
     // warp store covers 32 consecutive value channels of one token.
@@ -620,8 +667,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ok;
     };
 
+    // Chunks this CTA has run in earlier tasks: the per-chunk mbarriers
+    // complete once per chunk, so their phase is the parity of the running
+    // chunk count.
+    int gc = 0;
+    for (int ti = 0; ti < ntask && !failed; ti++) {
+    if (bal && ti > 0) set_task(ti);
+    if (tid == 0 && nchunks > 0) {
+        issue_qk(0);
+        issue_g(0);
+        if (!v_zero) issue_v(0);
+    }
+    beta_next = load_beta(0);
+    if (from_slot) {
+        // The head of this sequence ran first on the previous CTA; its final
+        // state is in the slot once the flag is set. The wait is bounded by
+        // far more than a head can take (at most nch chunks, ~5 us each).
+        bool waited = true;
+        if (tid == 0) {
+            const long long t0 = clock64(), limit = max(1LL << 31, (long long)nch << 22);
+            while (ld_acquire_gpu(p.bal_flags + bh) == 0) {
+                if (clock64() - t0 > limit) { waited = false; break; }
+            }
+        }
+        if (__syncthreads_or(!waited)) { failed = true; break; }
+    }
+    // Incoming state -> TMEM, transposed: lane j = value channel j, column i
+    // = key channel i (a warp reads 128 contiguous bytes of a state row per load).
+    {
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; e++) {
+            const int i = 32 * u + e;
+            x[e] = kind == 1 ? (lane == i ? 1.f : 0.f)
+                   : from_slot ? __ldcg(h0p + (size_t)i * kD + lane)
+                   : (h0p ? h0p[(size_t)i * kD + lane] : 0.f);
+        }
+        tmem_st16(tq + TM_S + 32 * u, x);
+        tmem_st16(tq + TM_S + 32 * u + 16, x + 16);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
     for (int c = 0; c < nchunks && !failed; c++) {
-        const uint32_t par = (uint32_t)(c & 1);
+        const uint32_t par = (uint32_t)((gc + c) & 1);
 
         // ------------------------------------------------------------ P1
         // Warp w owns channels 8w .. 8w + 7 of all four tiles; lane (a, j) =
@@ -1126,15 +1217,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (tid == kR2Thread) bulk_wait_all();
-    // Final state -> hT.
     // Final state: hT (whole sequences), the segment's zero-start state or
-    // its transition (segment pass), nothing (correction pass).
+    // its transition (segment pass), nothing (correction pass); in the
+    // balanced schedule a head's state goes to its handoff slot.
     float* hTp = nullptr;
     {
         int bh2, seg2;
         task_seq(&bh2, &seg2);
-        if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * kD * kD : nullptr;
+        if (bal) hTp = to_slot ? p.bal_states + (size_t)bh * kD * kD
+                       : p.hT  ? p.hT + (size_t)bh * kD * kD
+                               : nullptr;
+        else if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * kD * kD : nullptr;
         else if (p.pass == 3) hTp = p.ws_m + (size_t)bh2 * kD * kD;
         else if (p.pass == 4) hTp = nullptr;
         else if (kind == 0) hTp = p.ws_s0 + ((size_t)bh2 * p.nseg + seg2) * kD * kD;
@@ -1150,6 +1243,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < 16; jj++) dst[(size_t)(32 * u + cc + jj) * kD] = x[jj];
         }
     }
+    gc += nchunks;
+    // The next task overwrites the state in TMEM and the O staging rows.
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (to_slot && tid == 0 && !failed) {
+        __threadfence();
+        st_release_gpu(p.bal_flags + bh, 1);
+    }
+    }  // tasks
+    if (tid == kR2Thread) bulk_wait_all();
     report_flags(p.d_status, flags);
     tc_fence_before();
     __syncthreads();
@@ -1215,6 +1319,9 @@ TcParams base_params(const ChunkFwdArgs& a) {
     p.BH = a.B * a.H;
     p.ws_s0 = p.ws_m = nullptr;
     p.ws_sin = nullptr;
+    p.bal_W = 0;
+    p.bal_states = nullptr;
+    p.bal_flags = nullptr;
     return p;
 }
 
@@ -1230,10 +1337,62 @@ cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaSt
 
 }  // namespace
 
+// Balanced schedule (see TcParams::bal_W): when B * H sequences do not fill
+// whole waves of one CTA per SM, one cooperative launch of (at most) one CTA
+// per SM gives every CTA the same number of chunk steps. Returns
+// cudaErrorNotSupported when the plain schedule should run instead.
+cudaError_t launch_balanced(const TcMaps& m, const ChunkFwdArgs& a) {
+    if (!a.bal_ws || a.ckpt || a.T <= 0) return cudaErrorNotSupported;
+    int dev = 0, nsm = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kda_chunk_tc_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_chunk_tc_kernel<false>, kThreads,
+                                                      SMEM_BYTES) != cudaSuccess ||
+        nsm <= 0 || per_sm <= 0) {
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    const long long G = (long long)nsm * per_sm, BH = (long long)a.B * a.H;
+    const long long nch = (a.T + kC - 1) / kC;
+    if (BH <= G) return cudaErrorNotSupported;
+    const long long W = (BH * nch + G - 1) / G;  // > nch: a range holds at most one head and one tail
+    // Critical path in chunk steps: waves of whole sequences against W plus
+    // about two chunk steps for each of the (at most two) state handoffs.
+    const long long plain = ((BH + G - 1) / G) * nch;
+    if ((W + 4) * 100 >= plain * 97) return cudaErrorNotSupported;
+    TcParams p = base_params(a);
+    p.bal_W = (int)W;
+    p.bal_states = static_cast<float*>(a.bal_ws);
+    p.bal_flags = reinterpret_cast<int*>(static_cast<char*>(a.bal_ws) +
+                                         (size_t)BH * kD * kD * sizeof(float));
+    cudaError_t e = cudaMemsetAsync(p.bal_flags, 0, (size_t)BH * sizeof(int), a.stream);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((BH * nch + W - 1) / W));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: a tail may wait on a head
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kda_chunk_tc_kernel<false>, m.q, m.k, m.v, m.g, m.o, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
     if (a.dk != kD || a.dv != kD) return launch_chunk_fwd_simt(a, KDA_BF16);
     TcMaps m;
     if (!make_maps(&m, a)) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_balanced(m, a);
+    if (e != cudaErrorNotSupported) return e;
     return launch_tc<false>(m, base_params(a), (long long)a.B * a.H, a.stream);
 }
 

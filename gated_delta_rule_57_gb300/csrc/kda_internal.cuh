@@ -26,6 +26,9 @@ struct ChunkFwdArgs {
     cudaStream_t stream;
     float* ckpt = nullptr;  // [B, H, T / ckpt_every, dk, dv] or null
     int ckpt_every = 0;     // tokens between checkpoints (multiple of 64)
+    // balanced_workspace_bytes(B * H) bytes for the balanced schedule of the
+    // tensor-core prefill, or null (one CTA per sequence)
+    void* bal_ws = nullptr;
 };
 
 struct DecodeArgs {
@@ -78,6 +81,11 @@ cudaError_t launch_chunk_fwd_tc_slice(const ChunkFwdArgs& a, int which, float* s
 // slices 1..), hT [BH] (nullable).
 cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                               int nslice, cudaStream_t stream);
+// Handoff buffer of the balanced prefill schedule: one 128 x 128 fp32 state
+// and one int flag per sequence (flags rounded up to 256 bytes).
+inline size_t balanced_workspace_bytes(long long BH) {
+    return (size_t)BH * 128u * 128u * 4u + (((size_t)BH * 4u + 255u) & ~(size_t)255u);
+}
 inline size_t segmented_workspace_floats(long long BH, int nseg) {
     // per sequence: nseg zero-start final states, nseg - 1 transitions and
     // nseg - 1 incoming states, 128 x 128 fp32 each

@@ -89,9 +89,17 @@ const char* kda_status_string(kda_status_t s);
 const char* kda_last_error_string(void);
 
 /*
- * Bytes of device workspace kda_chunk_fwd needs for this problem. The current
- * kernels keep everything on chip and return 0; callers should still query it
- * and pass a buffer at least this large (NULL is accepted when it is 0).
+ * Bytes of device workspace that let kda_chunk_fwd balance the work over the
+ * SMs: B*H*dk*dv*4 bytes of states plus B*H ints (rounded up to 256 bytes) for
+ * io = KDA_BF16 with dk = dv = 128, T > 0 and B*H >= 2; 0 otherwise (the fp32
+ * path keeps nothing off chip). With a buffer of at least this size the
+ * tensor-core path may run one CTA per SM over the sequences laid end to end,
+ * a sequence split between two CTAs handing its state over through the
+ * buffer (it does so when B*H sequences would leave a partly filled last wave
+ * of one CTA per sequence). A smaller buffer or NULL is accepted and runs one
+ * CTA per sequence; both give bit-identical results. The buffer must be
+ * 16-byte aligned, must not overlap any other argument and must not be used by
+ * another call in flight; its contents need no initialisation.
  * Returns (size_t)-1 for arguments kda_chunk_fwd would reject.
  */
 size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dtype_t io);
@@ -119,7 +127,9 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
  *   stream : cudaStream_t
  *
  * io = KDA_BF16 runs the tensor-core (tcgen05/TMEM) path with fp32 state;
- * io = KDA_F32 runs an fp32 CUDA-core path for high-accuracy callers.
+ * io = KDA_F32 runs an fp32 CUDA-core path for high-accuracy callers. With a
+ * full-size workspace the tensor-core path enqueues a memset of the handoff
+ * flags before its (cooperative) launch.
  */
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
                            const float* beta, const float* h0, void* o, float* hT, int B,

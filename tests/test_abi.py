@@ -45,7 +45,13 @@ def test_status_enum_matches_header():
 
 
 def test_workspace_size(L):
-    assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 128, 128, kda.KDA_BF16) == 0
+    # the tensor-core path's handoff buffer for the balanced schedule: one
+    # 128 x 128 fp32 state and one int per sequence (ints padded to 256 bytes)
+    assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 128, 128, kda.KDA_BF16) == 256 * 65536 + 1024
+    assert L.kda_chunk_fwd_workspace_size(3, 64, 100, 128, 128, kda.KDA_BF16) == 300 * 65536 + 1280
+    assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 128, 128, kda.KDA_F32) == 0
+    assert L.kda_chunk_fwd_workspace_size(8, 0, 32, 128, 128, kda.KDA_BF16) == 0
+    assert L.kda_chunk_fwd_workspace_size(1, 64, 1, 128, 128, kda.KDA_BF16) == 0
     bad = ctypes.c_size_t(-1).value
     assert L.kda_chunk_fwd_workspace_size(1, 16, 1, 96, 96, kda.KDA_BF16) == bad
     assert L.kda_chunk_fwd_workspace_size(1, 16, 1, 128, 64, kda.KDA_F32) == bad
