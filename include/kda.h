@@ -126,8 +126,10 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
  *   d_status : device int or NULL              (in/out, OR-ed KDA_DEV_* bits)
  *   stream : cudaStream_t
  *
- * io = KDA_BF16 runs the tensor-core (tcgen05/TMEM) path with fp32 state;
- * io = KDA_F32 runs an fp32 CUDA-core path for high-accuracy callers. With a
+ * io = KDA_BF16 with dk = dv = 128 runs the tensor-core (tcgen05/TMEM) path
+ * with fp32 state; io = KDA_F32 (and bf16 with dk = dv = 64, whose tiles the
+ * tensor-core kernel does not implement) runs an fp32 CUDA-core path, untuned,
+ * meant for accuracy rather than speed. With a
  * full-size workspace the tensor-core path enqueues a memset of the handoff
  * flags before its (cooperative) launch.
  */
