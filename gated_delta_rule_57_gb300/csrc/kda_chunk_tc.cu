@@ -43,10 +43,11 @@
 // by TMA with the 128-byte swizzle (q, k, v in the layout the MMA descriptors
 // expect; g in 32-channel blocks); the next chunk's g, q/k, v and beta are
 // prefetched as soon as their buffers are free. Issuing a tcgen05.mma keeps
-// the issuing thread busy for about the product's duration, so rounds 1, 2
-// and 4 and the O store are issued by a thread of warp 15, whose own results
-// (P rows, a share of -Y) are needed only later in the chunk; thread 0
-// issues round 3. Completion is signalled through mbarriers whose waits are
+// the issuing thread busy for about the product's duration, so the rounds sit
+// on warps whose own results are needed only later in the chunk: warp 15
+// issues rounds 1 and 4 (and the next g tile), warp 12, which has no readout
+// rows, round 2 and the O store, thread 0 round 3 (every warp waits for it).
+// Completion is signalled through mbarriers whose waits are
 // bounded (timeout -> KDA_DEV_TIMEOUT). A CTA barrier stands only where a
 // phase reads other warps' results. The decay scan, the decay constants and
 // the operand build need none: each warp owns eight channels of all four
@@ -70,12 +71,12 @@ using namespace ptx;
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
 constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
-// Rounds 1, 2 and 4 and the O store are issued by warp 15 (issuing keeps a
+// Rounds 1 and 4 and the next g tile are issued by warp 15 (issuing keeps a
 // thread busy for about the MMA's duration; warp 15's other results are
 // needed only late in the chunk).
 constexpr int kIssueThread = kThreads - 32;
-// Round 2, the O store and the next g load: warp 12, which has no readout
-// rows and waits for round 2 itself.
+// Round 2 and the O store: warp 12, which has no readout rows and waits for
+// round 2 itself.
 constexpr int kR2Thread = 384;
 // The next chunk's q/k and v tiles are requested by warp 10, idle in the solve.
 constexpr int kTmaThread = 320;
