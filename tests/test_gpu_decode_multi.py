@@ -146,3 +146,46 @@ def test_multi_nonfinite_qkv_is_flagged(name):
                              status=status)
         torch.cuda.synchronize()
         assert int(status.item()) & kda.KDA_DEV_NONFINITE
+
+
+@pytest.mark.parametrize("io,d,K", [("bf16", 128, 8), ("f32", 128, 7), ("bf16", 64, 3),
+                                    ("f32", 64, 8)])
+def test_commit_with_outputs(io, d, K):
+    """A commit that also returns the outputs (every draft accepted, or a
+    per-sequence prefix): o of the accepted tokens and the state after them."""
+    N, H = 5, 3
+    x = draft(N, K, H, d, io, 29)
+    acc = [K, 1, K - 1, 2, K]
+    ntok = torch.tensor(acc, dtype=torch.int32, device=DEV)
+    S = x["h0"].clone()
+    o = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, ntok=ntok,
+                             commit=True)
+    torch.cuda.synchronize()
+    xc = {n: t.cpu() for n, t in x.items()}
+    for n, m in enumerate(acc):
+        sl = slice(n, n + 1)
+        o_ref, h_ref = oracle.prefill(xc["q"][sl, :m], xc["k"][sl, :m], xc["v"][sl, :m],
+                                      xc["g"][sl, :m], xc["beta"][sl, :m], xc["h0"][sl])
+        assert_o(o[sl, :m], o_ref, inputs.io_dtype(io), f"o of the {m} accepted tokens")
+        assert_s(S[sl], h_ref, inputs.io_dtype(io), f"state after {m} accepted tokens")
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_decay_at_its_bound_over_eight_drafts(io):
+    """g = -5 on every channel of eight drafts: the block forms scale by
+    e^{G} and e^{-G} with |G| up to 40, far inside fp32."""
+    N, K, H, d = 3, 8, 2, 128
+    x = draft(N, K, H, d, io, 30)
+    x["g"].fill_(-5.0)
+    S = x["h0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o_v = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, status=status)
+    o_c = kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, commit=True,
+                               status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    xc = {n: t.cpu() for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o_v, o_ref, inputs.io_dtype(io), "verify")
+    assert_o(o_c, o_ref, inputs.io_dtype(io), "commit")
+    assert_s(S, h_ref, inputs.io_dtype(io))
