@@ -10,8 +10,10 @@ The same run also times the batched decode workload (256 sequences x H=32,
 in the "decode" object, and a speculative-decoding round (verify + commit of 4
 draft tokens) in "spec_decode", and the long-context workload (B=1, T=2^20,
 H=32) single-pass and split in time into parallel segments in "prefill_long"
-(--no-long skips it), and the workload B=1, T=4096, H=32 (half the heads at
-g = -4.99) the same two ways in "prefill_t4k". Inputs are synthetic (seeded), already
+(--no-long skips it; the split by the shape-only segment hint, and as planned
+from a sampled decay statistic of g, probe and plan timed with the call), and
+the workload B=1, T=4096, H=32 (half the heads at g = -4.99) the same three
+ways in "prefill_t4k". Inputs are synthetic (seeded), already
 resident in HBM for `value`; `e2e` repeats the prefill step through the same
 C-ABI call from pinned host buffers, every input uploaded and o, hT read back
 inside the timed region, pipelined by batch row over copy and compute streams;
@@ -403,19 +405,27 @@ def time_spec_decode(device, seed, K=4, iters=50, warmup=5):
 
 def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
     """A workload with few sequences (B*H well below the SM count), timed in
-    one pass (kda_chunk_fwd) and split in time into the segment count
+    one pass (kda_chunk_fwd), split in time into the segment count
     kda_chunk_fwd_segments_hint picks (kda_chunk_fwd_segmented: segment
-    pass, scan, correction). Each call is timed alone with CUDA events; with
-    flush_l2 a 256 MB buffer is written before each timed call, so inputs
-    that fit in part in L2 start cold. Returns (single-pass ms, segmented ms,
-    nseg, launches per segmented call)."""
+    pass, scan, correction), and split as planned from the decay statistic
+    (kda_chunk_fwd_decay_probe, its B x 64 x H floats copied to the host,
+    kda_chunk_fwd_segments_hint_decay, then kda_chunk_fwd_segmented with that
+    nseg and lead: all of it inside each timed step). Each call is timed alone
+    with CUDA events; with flush_l2 a 256 MB buffer is written before each
+    timed call, so inputs that fit in part in L2 start cold. Returns
+    (single-pass ms, segmented ms, nseg, launches per segmented call,
+    decay-planned ms, its (nseg, lead) in the last timed step)."""
     from gated_delta_rule_57_gb300 import kda
     x = inputs.prefill_inputs(w, device, seed=seed)
     o = torch.empty_like(x["v"])
     hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=device)
     nseg = kda.kda_chunk_fwd_segments_hint(w.B, w.T, w.H, w.dk, w.dv)
+    nseg_max = min(32, (w.T + 63) // 64)
     ws = torch.empty(max(1, kda.kda_chunk_fwd_segmented_workspace_size(
-        w.B, w.T, w.H, w.dk, w.dv, nseg=nseg)), dtype=torch.uint8, device=device)
+        w.B, w.T, w.H, w.dk, w.dv, nseg=nseg_max)), dtype=torch.uint8, device=device)
+    probe = torch.empty(w.B, 64, w.H, dtype=torch.float32, device=device)
+    probe_h = torch.empty(w.B, 64, w.H, dtype=torch.float32).pin_memory()
+    planned = [None]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if flush_l2 else None
     stream = torch.cuda.current_stream()
 
@@ -427,8 +437,17 @@ def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
         kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
                                     nseg=nseg, o=o, hT=hT, workspace=ws, stream=stream)
 
+    def decay_planned():
+        kda.kda_chunk_fwd_decay_probe(x["g"], out=probe, stream=stream)
+        probe_h.copy_(probe, non_blocking=True)
+        stream.synchronize()
+        n, ld = kda.kda_chunk_fwd_segments_hint_decay(w.B, w.T, w.H, w.dk, w.dv, probe=probe_h)
+        planned[0] = (n, ld)
+        kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                    nseg=n, lead=ld, o=o, hT=hT, workspace=ws, stream=stream)
+
     res = []
-    for f in (single, segmented):
+    for f in (single, segmented, decay_planned):
         for _ in range(warmup):
             f()
         torch.cuda.synchronize()
@@ -444,15 +463,16 @@ def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
         res.append(statistics.mean(a.elapsed_time(b) for a, b in ev))
     del x, o, ws, flush
     torch.cuda.empty_cache()
-    return res[0], res[1], nseg, (3 if nseg > 1 else 1)
+    return res[0], res[1], nseg, (3 if nseg > 1 else 1), res[2], planned[0]
 
 
 def few_sequences_obj(w, device, rank, world, peaks, iters, warmup, flush_l2):
     """JSON object of time_single_and_segmented for workload w."""
-    t1, ts, nseg, launches = time_single_and_segmented(w, device, rank_seed(w.seed, rank), iters,
-                                                       warmup, flush_l2)
+    t1, ts, nseg, launches, td, (nd, ld) = time_single_and_segmented(
+        w, device, rank_seed(w.seed, rank), iters, warmup, flush_l2)
     t1 = max_over_ranks(t1, world, device)
     ts = max_over_ranks(ts, world, device)
+    td = max_over_ranks(td, world, device)
     nbytes = prefill_bytes(w)
     tok = w.B * w.T
     return {
@@ -464,7 +484,15 @@ def few_sequences_obj(w, device, rank, world, peaks, iters, warmup, flush_l2):
                       "unit": "tokens/s",
                       "frac_of_peak_hbm": nbytes / (ts * 1e-3) / 1e9 / peaks["hbm_gbs"],
                       "launches_per_step": launches},
+        "segmented_decay_planned": {
+            "nseg": nd, "lead": ld, "ms_per_step": td, "value": job_value(tok, td, world),
+            "unit": "tokens/s",
+            "frac_of_peak_hbm": nbytes / (td * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "launches_per_step": 1 + (3 if nd > 1 else 1),
+            "what": "decay probe of g, its result read back on the host, plan, segmented "
+                    "call: all inside the timed step"},
         "speedup": t1 / ts,
+        "speedup_decay_planned": t1 / td,
         "algorithmic_bytes_per_step": nbytes,
         "l2": ("256 MB written between timed calls" if flush_l2
                else f"inputs larger than L2 ({nbytes / 1e9:.1f} GB per step)"),

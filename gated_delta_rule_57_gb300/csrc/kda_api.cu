@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -161,12 +163,28 @@ int device_sms() {
 // segment pass starts the BH long first segments, the other SMs take the
 // 2 BH (nseg - 1) short runs (segments from zero and transitions) and every
 // SM joins once the long runs end; the correction pass has BH (nseg - 1)
-// short runs. Returns -1 when the split leaves empty segments.
-long long split_cost(long long BH, int T, int nseg, int lead, int nsm) {
+// short runs. tl < 0: the runs with v = 0 (transitions, corrections) take
+// their whole segment; else about tl chunks (they stop once their state is
+// exactly zero). Returns -1 when the split leaves empty segments.
+long long split_cost(long long BH, int T, int nseg, int lead, int nsm, long long tl = -1) {
     int sc, se;
     segment_shape(T, nseg, lead, &sc, &se);
     if (se != nseg) return -1;
     auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
+    if (tl >= 0 && tl < sc) {
+        // The BH (nseg - 1) segments from zero run sc chunks each, the
+        // transitions (dispatched after them) and corrections about tl.
+        const long long z = BH * (nseg - 1);
+        long long p1;
+        if (BH >= nsm) {
+            p1 = waves(BH) * lead * sc + waves(z) * (sc + tl);
+        } else {
+            const long long free_sms = nsm - BH, wz = (z + free_sms - 1) / free_sms;
+            p1 = wz <= lead ? std::max((long long)lead * sc, wz * (sc + tl))
+                            : ((long long)lead + waves(z - free_sms * lead)) * sc + waves(z) * tl;
+        }
+        return p1 + waves(z) * tl;
+    }
     const long long shorts = 2 * BH * (nseg - 1);
     long long p1;
     if (BH >= nsm) {
@@ -184,13 +202,13 @@ long long split_cost(long long BH, int T, int nseg, int lead, int nsm) {
 // SMs: the cheapest of 1 .. 16 that leaves as many non-empty segments as an
 // even split (so the workspace does not depend on the device); 1 without a
 // device (nsm = 0).
-int choose_lead(long long BH, int T, int nseg, int nsm) {
+int choose_lead(long long BH, int T, int nseg, int nsm, long long tl = -1) {
     if (nseg <= 1 || nsm <= 0) return 1;
     int best = 1;
-    long long best_cost = split_cost(BH, T, nseg, 1, nsm);
+    long long best_cost = split_cost(BH, T, nseg, 1, nsm, tl);
     if (best_cost < 0) return 1;
     for (int lead = 2; lead <= 16; lead++) {
-        const long long c = split_cost(BH, T, nseg, lead, nsm);
+        const long long c = split_cost(BH, T, nseg, lead, nsm, tl);
         if (c >= 0 && c < best_cost) {
             best_cost = c;
             best = lead;
@@ -205,7 +223,7 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
                             int ckpt_every, int* d_status, void* stream, int nseg = 1,
                             void* workspace = nullptr, size_t ws_bytes = 0,
                             bool check_only = false, void* bal_ws = nullptr,
-                            size_t bal_bytes = 0) {
+                            size_t bal_bytes = 0, int lead_in = 0) {
     if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
     kda_status_t st = check_dims(dk, dv, io);
     if (st != KDA_OK) return st;
@@ -257,8 +275,10 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
         const int nch = (T + 63) / 64;
         if (nseg < 1 || (T > 0 && nseg > nch))
             return fail(KDA_ERR_INVALID_ARG, "nseg must be in 1 .. ceil(T / 64)");
+        if (lead_in > 0 && T > 0 && lead_in > nch)
+            return fail(KDA_ERR_INVALID_ARG, "lead must be <= 0 (the library's choice) or in 1 .. ceil(T / 64)");
         segment_shape(T, nseg, 1, &seg_chunks, &nseg_eff);
-        lead = choose_lead((long long)B * H, T, nseg_eff, device_sms());
+        lead = lead_in > 0 ? lead_in : choose_lead((long long)B * H, T, nseg_eff, device_sms());
         segment_shape(T, nseg_eff, lead, &seg_chunks, &nseg_eff);
     }
     // Every argument but the workspace is valid.
@@ -366,17 +386,91 @@ int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t
     return best_cost >= 0 && best_cost * 5 < base * 4 ? best : 1;
 }
 
+int kda_chunk_fwd_segments_hint_decay(int B, int T, int H, int dk, int dv, kda_dtype_t io,
+                                      const float* probe, int nprobe, int* lead) {
+    if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return -1;
+    if ((long long)B * H >= (1LL << 31)) return -1;
+    if (nprobe < 0 || (nprobe > 0 && !probe)) return -1;
+    if (lead) *lead = 1;
+    if (io != KDA_BF16 || dk != 128 || B == 0 || H == 0) return 1;
+    const int nsm = device_sms();
+    if (nsm == 0) return 1;
+    // The weakest decay per chunk the sample shows; a run with v = 0 loses
+    // at least that much (log scale) per chunk, and is exactly zero once the
+    // total passes fp32's smallest subnormal (2^-149 = e^-103.28), one chunk
+    // later it has stopped. No sample, a non-negative or non-finite entry:
+    // count the runs as whole segments, as kda_chunk_fwd_segments_hint does.
+    float cd = nprobe > 0 ? -INFINITY : 0.f;
+    for (int i = 0; i < nprobe; i++) {
+        if (!std::isfinite(probe[i])) {
+            cd = 0.f;
+            break;
+        }
+        cd = std::max(cd, probe[i]);
+    }
+    const long long BH = (long long)B * H, nch = (T + 63) / 64;
+    long long tl = -1;
+    if (cd < 0.f) tl = std::min<long long>(nch, 2 + (long long)std::ceil(103.28f / -cd));
+    const long long base = ((BH + nsm - 1) / nsm) * nch;
+    int best = 1, best_lead = 1;
+    long long best_cost = -1;
+    for (int s = 2; s <= 32 && s <= nch; s++) {
+        int sc, se;
+        segment_shape(T, s, 1, &sc, &se);
+        if (se != s) continue;
+        const int ld = choose_lead(BH, T, s, nsm, tl);
+        const long long c = split_cost(BH, T, s, ld, nsm, tl);
+        if (c < 0) continue;
+        const long long cost = c + (s - 1);
+        if (best_cost < 0 || cost * 50 < best_cost * 49) {
+            best_cost = cost;
+            best = s;
+            best_lead = ld;
+        }
+    }
+    if (!(best_cost >= 0 && best_cost * 5 < base * 4)) return 1;
+    if (lead) *lead = best_lead;
+    return best;
+}
+
+kda_status_t kda_chunk_fwd_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
+                                       float* d_probe, void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd_decay_probe");
+    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "B, T, H must be >= 0");
+    if (dk != 64 && dk != 128) return fail(KDA_ERR_UNSUPPORTED, "dk must be 64 or 128");
+    if (nsample < 1 || nsample > 4096) return fail(KDA_ERR_INVALID_ARG, "nsample must be in 1 .. 4096");
+    if ((long long)B * H >= (1LL << 31) || B > 65535 || H > 8 * 65535)
+        return fail(KDA_ERR_INVALID_ARG, "B must be <= 65535, H <= 524280 and B*H < 2^31");
+    if (B == 0 || H == 0 || T == 0) return KDA_OK;
+    size_t n_g, n_p;
+    if (!mul_ok(&n_g, B, T, H, dk) || !mul_ok(&n_p, B, nsample, H))
+        return fail(KDA_ERR_INVALID_ARG, "tensor size overflow");
+    if (!g || !d_probe) return fail(KDA_ERR_INVALID_ARG, "g and d_probe must be non-NULL");
+    if (!aligned16(g) || !aligned4(d_probe))
+        return fail(KDA_ERR_INVALID_ARG, "g must be 16-byte and d_probe 4-byte aligned");
+    if (overlaps(d_probe, n_p * 4, g, n_g * 4))
+        return fail(KDA_ERR_INVALID_ARG, "d_probe overlaps g");
+    cudaError_t e = kda::launch_decay_probe(g, B, T, H, dk, nsample, d_probe,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_last_error(cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 int kda_chunk_fwd_segment_plan(int B, int T, int H, int dk, int dv, kda_dtype_t io, int nseg,
-                               int* seg_chunks, int* lead) {
+                               int lead_in, int* seg_chunks, int* lead) {
     if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return -1;
     if ((long long)B * H >= (1LL << 31)) return -1;
     const int nch = (T + 63) / 64;
     if (nseg < 1 || (T > 0 && nseg > nch)) return -1;
     if (nseg > 1 && (io != KDA_BF16 || dk != 128)) return -1;
+    if (nseg > 1 && lead_in > 0 && T > 0 && lead_in > nch) return -1;
     int sc = nch, se = 1, ld = 1;
     if (nseg > 1) {
         segment_shape(T, nseg, 1, &sc, &se);
-        ld = choose_lead((long long)B * H, T, se, device_sms());
+        ld = lead_in > 0 ? lead_in : choose_lead((long long)B * H, T, se, device_sms());
         segment_shape(T, se, ld, &sc, &se);
     }
     if (seg_chunks) *seg_chunks = se > 1 ? sc : nch;
@@ -399,22 +493,23 @@ size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int d
 kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v,
                                      const float* g, const float* beta, const float* h0, void* o,
                                      float* hT, int B, int T, int H, int dk, int dv,
-                                     kda_dtype_t io, int nseg, void* workspace, size_t ws_bytes,
-                                     int* d_status, void* stream) {
+                                     kda_dtype_t io, int nseg, int lead, void* workspace,
+                                     size_t ws_bytes, int* d_status, void* stream) {
     NvtxRange nvtx_range("kda_chunk_fwd_segmented");
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0, d_status,
-                          stream, nseg, workspace, ws_bytes);
+                          stream, nseg, workspace, ws_bytes, false, nullptr, 0, lead);
 }
 
 kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
                                              const float* g, const float* beta, const float* h0,
                                              void* o, float* hT, int B, int T, int H, int dk,
-                                             int dv, kda_dtype_t io, int nseg, int* d_status,
-                                             void* stream) {
+                                             int dv, kda_dtype_t io, int nseg, int lead,
+                                             int* d_status, void* stream) {
     NvtxRange nvtx_range("kda_chunk_fwd_segmented_noalloc");
     // Argument errors first, as for the other entry points.
     kda_status_t st = chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr,
-                                     0, d_status, stream, nseg, nullptr, 0, /*check_only=*/true);
+                                     0, d_status, stream, nseg, nullptr, 0, /*check_only=*/true,
+                                     nullptr, 0, lead);
     if (st != KDA_OK) return st;
     const size_t need = kda_chunk_fwd_segmented_workspace_size(B, T, H, dk, dv, io, nseg);
     if (need > sizeof(g_seg_scratch))
@@ -428,7 +523,8 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
         }
     }
     return chunk_fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, H, dk, dv, io, nullptr, 0, d_status,
-                          stream, nseg, ws, need > 0 ? sizeof(g_seg_scratch) : 0);
+                          stream, nseg, ws, need > 0 ? sizeof(g_seg_scratch) : 0, false, nullptr,
+                          0, lead);
 }
 
 namespace {

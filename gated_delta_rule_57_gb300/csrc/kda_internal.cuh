@@ -81,6 +81,11 @@ cudaError_t launch_chunk_fwd_tc_slice(const ChunkFwdArgs& a, int which, float* s
 // slices 1..), hT [BH] (nullable).
 cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                               int nslice, cudaStream_t stream);
+// Sampled decay bound for planning a split in time: out[b][s][h] = sum over
+// the tokens of chunk floor(s * nch / nsample) of max over channels of
+// g[b][t][h][:] (g [B][T][H][dk] fp32, dk = 64 or 128).
+cudaError_t launch_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
+                               float* out, cudaStream_t stream);
 // Handoff buffer of the balanced prefill schedule: one 128 x 128 fp32 state
 // and one int flag per sequence (flags rounded up to 256 bytes).
 inline size_t balanced_workspace_bytes(long long BH) {

@@ -80,20 +80,26 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
                                              I, vp, vp]
             L.kda_chunk_fwd_ckpt.restype = I
             L.kda_chunk_fwd_segmented.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I,
-                                                  I, I, vp, sz, vp, vp]
+                                                  I, I, I, vp, sz, vp, vp]
             L.kda_chunk_fwd_segmented.restype = I
             L.kda_chunk_fwd_segmented_workspace_size.argtypes = [I, I, I, I, I, I, I]
             L.kda_chunk_fwd_segmented_workspace_size.restype = sz
             L.kda_chunk_fwd_segmented_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I,
-                                                          I, I, I, I, I, vp, vp]
+                                                          I, I, I, I, I, I, vp, vp]
             L.kda_chunk_fwd_segmented_noalloc.restype = I
             L.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp, vp]
             L.kda_selftest_wait_timeout.restype = I
             L.kda_chunk_fwd_segments_hint.argtypes = [I, I, I, I, I, I]
             L.kda_chunk_fwd_segments_hint.restype = I
-            L.kda_chunk_fwd_segment_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
+            L.kda_chunk_fwd_segment_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(I),
                                                      ctypes.POINTER(I)]
             L.kda_chunk_fwd_segment_plan.restype = I
+            L.kda_chunk_fwd_segments_hint_decay.argtypes = [I, I, I, I, I, I,
+                                                            ctypes.POINTER(ctypes.c_float), I,
+                                                            ctypes.POINTER(I)]
+            L.kda_chunk_fwd_segments_hint_decay.restype = I
+            L.kda_chunk_fwd_decay_probe.argtypes = [vp, I, I, I, I, I, vp, vp]
+            L.kda_chunk_fwd_decay_probe.restype = I
             L.kda_chunk_fwd_slice_transition.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp,
                                                          vp]
             L.kda_chunk_fwd_slice_transition.restype = I
@@ -182,13 +188,45 @@ def kda_chunk_fwd_segments_hint(B: int, T: int, H: int, dk: int, dv: int,
     return int(n)
 
 
+def kda_chunk_fwd_decay_probe(g, nsample: int = 64, out=None, stream=None):
+    """Sampled decay statistic of g [B,T,H,dk] for kda_chunk_fwd_segments_hint_decay:
+    a [B, nsample, H] fp32 device tensor (per head, the sum over a sampled
+    chunk's tokens of the max over channels of g)."""
+    B, T, H, dk = g.shape
+    if out is None:
+        out = torch.empty((B, nsample, H), dtype=torch.float32, device=g.device)
+    _check(lib().kda_chunk_fwd_decay_probe(_ptr(g), B, T, H, dk, nsample, _ptr(out),
+                                           _stream(stream)))
+    return out
+
+
+def kda_chunk_fwd_segments_hint_decay(B: int, T: int, H: int, dk: int, dv: int,
+                                      io: torch.dtype = torch.bfloat16, probe=None):
+    """(nseg, lead) for kda_chunk_fwd_segmented, planned with the decay
+    statistic `probe` (kda_chunk_fwd_decay_probe's output; a device tensor is
+    copied to the host first, which waits for it)."""
+    p = torch.as_tensor(probe if probe is not None else [], dtype=torch.float32)
+    p = p.detach().to("cpu").contiguous().reshape(-1)
+    ld = ctypes.c_int(1)
+    n = lib().kda_chunk_fwd_segments_hint_decay(
+        B, T, H, dk, dv, _DTYPE[io],
+        ctypes.cast(p.data_ptr(), ctypes.POINTER(ctypes.c_float)) if p.numel() else None,
+        p.numel(), ctypes.byref(ld))
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size")
+    return int(n), int(ld.value)
+
+
 def kda_chunk_fwd_segment_plan(B: int, T: int, H: int, dk: int, dv: int,
-                               io: torch.dtype = torch.bfloat16, nseg: int = 1):
-    """The split kda_chunk_fwd_segmented uses for nseg on this device:
-    (segments, seg_chunks, lead). Segment 0 spans lead * seg_chunks 64-token
-    chunks, each later segment seg_chunks (the last may be shorter)."""
+                               io: torch.dtype = torch.bfloat16, nseg: int = 1,
+                               lead: Optional[int] = None):
+    """The split kda_chunk_fwd_segmented uses for nseg (and lead; None: the
+    library's choice) on this device: (segments, seg_chunks, lead). Segment 0
+    spans lead * seg_chunks 64-token chunks, each later segment seg_chunks
+    (the last may be shorter)."""
     sc, ld = ctypes.c_int(0), ctypes.c_int(0)
-    n = lib().kda_chunk_fwd_segment_plan(B, T, H, dk, dv, _DTYPE[io], nseg, ctypes.byref(sc),
+    n = lib().kda_chunk_fwd_segment_plan(B, T, H, dk, dv, _DTYPE[io], nseg,
+                                         0 if lead is None else lead, ctypes.byref(sc),
                                          ctypes.byref(ld))
     if n < 0:
         raise KdaError(KDA_ERR_INVALID_ARG, "unsupported problem size or nseg")
@@ -204,11 +242,14 @@ def kda_chunk_fwd_segmented_workspace_size(B: int, T: int, H: int, dk: int, dv: 
     return int(n)
 
 
-def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg: Optional[int] = None, o=None,
-                            hT=None, want_hT: bool = True, status: Optional[torch.Tensor] = None,
-                            workspace=None, stream=None):
+def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg=None,
+                            lead: Optional[int] = None, o=None, hT=None, want_hT: bool = True,
+                            status: Optional[torch.Tensor] = None, workspace=None, stream=None):
     """kda_chunk_fwd with each sequence split in time into `nseg` segments run
-    in parallel (None: the library's hint for this device). Returns (o, hT)."""
+    in parallel, the first spanning `lead` segment lengths. nseg None: the
+    library's shape-only hint for this device; nseg "decay": plan with
+    kda_chunk_fwd_decay_probe of g (a host round trip that waits for the
+    probe). lead None: the library's choice for nseg. Returns (o, hT)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     io = _DTYPE.get(q.dtype)
@@ -216,6 +257,12 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg: Optional[int] = 
         raise TypeError(f"unsupported q dtype {q.dtype}")
     if nseg is None:
         nseg = kda_chunk_fwd_segments_hint(B, T, H, dk, dv, q.dtype)
+    elif nseg == "decay":
+        probe = kda_chunk_fwd_decay_probe(g, stream=stream)
+        with torch.cuda.stream(stream):  # the copy waits for the probe on its stream
+            host = probe.to("cpu")
+        nseg, ld = kda_chunk_fwd_segments_hint_decay(B, T, H, dk, dv, q.dtype, host)
+        lead = ld if lead is None else lead
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_hT:
@@ -226,14 +273,16 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg: Optional[int] = 
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     code = lib().kda_chunk_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                          _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, io, nseg,
-                                         _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+                                         0 if lead is None else lead, _ptr(workspace), ws_bytes,
+                                         _ptr(status), _stream(stream))
     _check(code)
     return o, hT
 
 
-def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, h0=None, *, nseg: int, o=None,
-                                    hT=None, want_hT: bool = True,
-                                    status: Optional[torch.Tensor] = None, stream=None):
+def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, h0=None, *, nseg: int,
+                                    lead: Optional[int] = None, o=None, hT=None,
+                                    want_hT: bool = True, status: Optional[torch.Tensor] = None,
+                                    stream=None):
     """kda_chunk_fwd_segmented with the library's static scratch (no workspace)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -246,7 +295,8 @@ def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, h0=None, *, nseg: int, o=N
         hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     code = lib().kda_chunk_fwd_segmented_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                                  _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, io,
-                                                 nseg, _ptr(status), _stream(stream))
+                                                 nseg, 0 if lead is None else lead, _ptr(status),
+                                                 _stream(stream))
     _check(code)
     return o, hT
 

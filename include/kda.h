@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 typedef enum {
     KDA_OK = 0,
@@ -180,6 +180,13 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
  *               correction, may span several segment lengths so that its long
  *               runs overlap the other segments' passes on the remaining SMs
  *               (kda_chunk_fwd_segment_plan gives the split for the device)
+ *   lead      : the first segment's length in segment lengths, 1 ..
+ *               ceil(T / 64), or <= 0 for the library's choice (the length
+ *               kda_chunk_fwd_segment_plan reports for lead <= 0); a lead
+ *               that leaves fewer non-empty segments runs fewer.
+ *               kda_chunk_fwd_segments_hint_decay suggests nseg and lead
+ *               together. The results do not depend on the split beyond
+ *               rounding.
  *   workspace : device buffer of kda_chunk_fwd_segmented_workspace_size bytes,
  *               16-byte aligned, not overlapping any other tensor; contents
  *               are scratch
@@ -193,8 +200,8 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
 kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v,
                                      const float* g, const float* beta, const float* h0, void* o,
                                      float* hT, int B, int T, int H, int dk, int dv,
-                                     kda_dtype_t io, int nseg, void* workspace, size_t ws_bytes,
-                                     int* d_status, void* stream);
+                                     kda_dtype_t io, int nseg, int lead, void* workspace,
+                                     size_t ws_bytes, int* d_status, void* stream);
 
 /*
  * Bytes of workspace kda_chunk_fwd_segmented needs: (3 nseg' - 2) * dk * dv * 4
@@ -235,8 +242,8 @@ size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int d
 kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
                                              const float* g, const float* beta, const float* h0,
                                              void* o, float* hT, int B, int T, int H, int dk,
-                                             int dv, kda_dtype_t io, int nseg, int* d_status,
-                                             void* stream);
+                                             int dv, kda_dtype_t io, int nseg, int lead,
+                                             int* d_status, void* stream);
 
 /*
  * Segment count that minimises the number of chunk steps on the critical
@@ -248,18 +255,62 @@ kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const
 int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t io);
 
 /*
- * The split kda_chunk_fwd_segmented uses for nseg on the current device:
- * returns the number of segments that results (1 = no split), or -1 for
- * arguments kda_chunk_fwd_segmented would reject. *seg_chunks (if not NULL)
+ * Sampled decay statistic for planning a split in time. A run with v = 0 (a
+ * segment's transition from the identity, a correction from its incoming
+ * state) multiplies its state token by token by (I - b k k^T) Diag(e^g); for
+ * unit keys and 0 <= b <= 2 the first factor is a contraction, so over a
+ * 64-token chunk the state's entries shrink at least by
+ * e^{sum_t max_c g[t, c]}, and once they pass fp32's smallest subnormal the
+ * state is exactly zero and the segmented prefill stops that run. This call
+ * writes d_probe[(b * nsample + s) * H + h] = sum_t max_c g[b, t, h, c] over
+ * the tokens t of chunk floor(s * nch / nsample) of batch row b
+ * (nch = ceil(T / 64); a short last chunk sums its tokens only).
+ *   g        : [B, T, H, dk] fp32 device, 16-byte aligned (the prefill's g)
+ *   nsample  : chunks sampled per batch row, 1 .. 4096
+ *   d_probe  : device, B * nsample * H floats, 4-byte aligned, not
+ *              overlapping g
+ * One launch of B * nsample * ceil(H / 8) CTAs on `stream`, one warp per
+ * (sample, row, head) reading that head's 64 rows of dk floats; nothing
+ * written when B, H or T is 0. dk must be 64 or 128 (KDA_ERR_UNSUPPORTED),
+ * B <= 65535, H <= 524280. The statistic guides the plan only: the results
+ * of the segmented call never depend on it.
+ */
+kda_status_t kda_chunk_fwd_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
+                                       float* d_probe, void* stream);
+
+/*
+ * kda_chunk_fwd_segments_hint with a decay statistic: probe (host memory,
+ * nprobe floats, e.g. a copy of kda_chunk_fwd_decay_probe's output) gives the
+ * decay per chunk the sequences can be counted on (its largest entry, cd).
+ * With cd < 0 the planner counts each transition and correction run as
+ * stopping after about 2 + ceil(103.28 / -cd) chunks instead of running its
+ * whole segment, which favours more, shorter segments and a shorter first
+ * one; with no entries, an entry >= 0 or a non-finite entry it plans as
+ * kda_chunk_fwd_segments_hint. Returns the segment count (1 = do not split)
+ * and writes the matching lead to *lead (if not NULL; 1 when it returns 1);
+ * pass both to kda_chunk_fwd_segmented. A sample that misses slowly decaying
+ * stretches makes those runs longer than planned: slower, never different
+ * results. -1 for arguments kda_chunk_fwd would reject, nprobe < 0 or a NULL
+ * probe with nprobe > 0.
+ */
+int kda_chunk_fwd_segments_hint_decay(int B, int T, int H, int dk, int dv, kda_dtype_t io,
+                                      const float* probe, int nprobe, int* lead);
+
+/*
+ * The split kda_chunk_fwd_segmented uses for nseg and lead_in (its lead
+ * argument; <= 0: the library's choice) on the current device: returns the
+ * number of segments that results (1 = no split), or -1 for arguments
+ * kda_chunk_fwd_segmented would reject. *seg_chunks (if not NULL)
  * receives the length of every segment after the first in 64-token chunks
  * (the last may be shorter; ceil(T / 64) when there is no split) and *lead
  * (if not NULL) the first segment's length in those units. The first segment
- * length is the one of 1 .. 16 that minimises the chunk steps on the critical
- * path when the segment pass starts the first segments' long runs on B * H
- * SMs and the other runs on the rest; 1 when no CUDA device is visible.
+ * length is lead_in when positive, else the one of 1 .. 16 that minimises
+ * the chunk steps on the critical path when the segment pass starts the
+ * first segments' long runs on B * H SMs and the other runs on the rest,
+ * counting every run as its whole segment; 1 when no CUDA device is visible.
  */
 int kda_chunk_fwd_segment_plan(int B, int T, int H, int dk, int dv, kda_dtype_t io, int nseg,
-                               int* seg_chunks, int* lead);
+                               int lead_in, int* seg_chunks, int* lead);
 
 /*
  * Building blocks for one long sequence split in time across devices (or

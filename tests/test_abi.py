@@ -188,8 +188,8 @@ def test_segment_plan(L):
     f.restype = ctypes.c_int
     sc, lead = ctypes.c_int(0), ctypes.c_int(0)
 
-    def plan(B, T, H, nseg, dk=128, io=kda.KDA_BF16):
-        return f(B, T, H, dk, dk, io, nseg, ctypes.byref(sc), ctypes.byref(lead))
+    def plan(B, T, H, nseg, dk=128, io=kda.KDA_BF16, lead_in=0):
+        return f(B, T, H, dk, dk, io, nseg, lead_in, ctypes.byref(sc), ctypes.byref(lead))
 
     # covers the chunks with the workspace's segment count, whatever the lead
     for B, T, H, nseg in ((1, 1 << 20, 32, 10), (1, 1000, 2, 7), (1, 2048, 32, 8), (2, 640, 3, 10)):
@@ -209,13 +209,61 @@ def test_segment_plan(L):
     assert plan(1, 4096, 32, 2, io=kda.KDA_F32) == -1
     assert plan(1, 4096, 32, 2, dk=64) == -1
     assert plan(-1, 4096, 32, 2) == -1
-    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 4, None, None) == 4  # outputs optional
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 4, 0, None, None) == 4  # outputs optional
+    # an explicit lead: the first segment spans lead segment lengths
+    assert plan(1, 1 << 20, 32, 16, lead_in=4) == 16 and lead.value == 4 and sc.value == 863
+    assert plan(1, 1 << 20, 32, 8, lead_in=2) == 8 and (lead.value, sc.value) == (2, 1821)
+    assert plan(1, 4096, 32, 16, lead_in=4) == 13 and (lead.value, sc.value) == (4, 4)
+    assert plan(1, 4096, 32, 2, lead_in=64) == 1  # the first segment covers everything
+    assert plan(1, 4096, 32, 2, lead_in=65) == -1  # longer than the sequence
 
 
-def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A[0]):
+def test_segments_hint_decay(L):
+    f = L.kda_chunk_fwd_segments_hint_decay
+    f.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int)]
+    probe = (ctypes.c_float * 3)(-30.0, -25.0, -40.0)
+    lead = ctypes.c_int(7)
+    n = f(1, 1 << 20, 32, 128, 128, kda.KDA_BF16, probe, 3, ctypes.byref(lead))
+    assert 1 <= n <= 32 and lead.value >= 1  # 1 and 1 without a visible GPU
+    assert f(1, 4096, 32, 128, 128, kda.KDA_F32, probe, 3, ctypes.byref(lead)) == 1
+    assert lead.value == 1
+    assert f(1, 4096, 32, 96, 96, kda.KDA_BF16, probe, 3, None) == -1
+    assert f(-1, 4096, 32, 128, 128, kda.KDA_BF16, probe, 3, None) == -1
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, None, 3, None) == -1   # no probe
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, probe, -1, None) == -1
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, None, 0, None) >= 1    # empty sample
+
+
+def call_probe(L, g=A[3], B=1, T=128, H=1, dk=128, nsample=4, out=A[6]):
+    L.kda_chunk_fwd_decay_probe.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 5 + \
+        [ctypes.c_void_p, ctypes.c_void_p]
+    return L.kda_chunk_fwd_decay_probe(g, B, T, H, dk, nsample, out, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), ST.KDA_ERR_INVALID_ARG),
+    (dict(dk=96), ST.KDA_ERR_UNSUPPORTED),
+    (dict(nsample=0), ST.KDA_ERR_INVALID_ARG),
+    (dict(nsample=4097), ST.KDA_ERR_INVALID_ARG),
+    (dict(B=65536), ST.KDA_ERR_INVALID_ARG),
+    (dict(g=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(out=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(g=A[3] + 2), ST.KDA_ERR_INVALID_ARG),   # misaligned
+    (dict(g=A[3] + 4), ST.KDA_ERR_INVALID_ARG),   # g not 16-byte aligned
+    (dict(H=8 * 65535 + 1, T=1, B=1), ST.KDA_ERR_INVALID_ARG),
+    (dict(out=A[3] + 64), ST.KDA_ERR_INVALID_ARG),  # inside g
+    (dict(B=0), ST.KDA_OK),                        # nothing to do: no launch
+    (dict(T=0), ST.KDA_OK),
+])
+def test_decay_probe_rejects(L, kw, code):
+    assert call_probe(L, **kw) == code
+
+
+def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A[0], lead=0):
     # T = 128: two chunks; every tensor fits the 64 KB spacing of the fake addresses
     return L.kda_chunk_fwd_segmented(q, A[1], A[2], A[3], A[4], None, A[5], A[6], 1, T, 1, dk,
-                                     dk, io, nseg, ws, ws_bytes, None, None)
+                                     dk, io, nseg, lead, ws, ws_bytes, None, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -228,6 +276,7 @@ def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A
     (dict(ws=A[7] + 8, ws_bytes=1 << 22), ST.KDA_ERR_INVALID_ARG),  # misaligned
     (dict(ws=A[0], ws_bytes=1 << 22), ST.KDA_ERR_INVALID_ARG),    # overlaps q
     (dict(q=None), ST.KDA_ERR_INVALID_ARG),
+    (dict(lead=3), ST.KDA_ERR_INVALID_ARG),                       # longer than the 2 chunks
 ])
 def test_segmented_rejects(L, kw, code):
     assert call_seg(L, **kw) == code

@@ -108,9 +108,11 @@ def test_segmented_nonfinite_qkv_is_flagged(name):
 @pytest.mark.slow
 def test_t1m_benchmark_calls_against_oracle():
     """The long-context workload (B=1, T=2^20, H=32, the benchmark's seed)
-    through the two calls the benchmark times: kda_chunk_fwd in one pass and
+    through the three calls the benchmark times: kda_chunk_fwd in one pass,
     kda_chunk_fwd_segmented with the segment count of
-    kda_chunk_fwd_segments_hint and the library's first-segment length. The
+    kda_chunk_fwd_segments_hint and the library's first-segment length, and
+    kda_chunk_fwd_segmented planned from kda_chunk_fwd_decay_probe (more,
+    shorter segments, in a workspace sized for 32). The
     oracle recomputes four heads (two of them apart by half the head range)
     over the whole sequence, and every output and the final state of those
     heads is checked for both calls, so the transitions built over the long
@@ -141,6 +143,21 @@ def test_t1m_benchmark_calls_against_oracle():
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got["segmented"] = (o[:, :, heads].cpu(), hT[:, heads].cpu())
+    del ws
+    ws = torch.empty(kda.kda_chunk_fwd_segmented_workspace_size(w.B, w.T, w.H, w.dk, w.dv,
+                                                                nseg=32),
+                     dtype=torch.uint8, device=DEV)
+    probe = kda.kda_chunk_fwd_decay_probe(x["g"])
+    nseg_d, lead_d = kda.kda_chunk_fwd_segments_hint_decay(w.B, w.T, w.H, w.dk, w.dv,
+                                                           probe=probe)
+    assert nseg_d > nseg, (nseg_d, lead_d)  # this decay empties a state within a few chunks
+    o.fill_(float("nan"))
+    hT.fill_(float("nan"))
+    kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], None, nseg="decay",
+                                o=o, hT=hT, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got["segmented_decay"] = (o[:, :, heads].cpu(), hT[:, heads].cpu())
     sub = {n: x[n][:, :, heads].contiguous().cpu() for n in ("q", "k", "v", "g", "beta")}
     del x, o, hT, ws
     torch.cuda.empty_cache()
@@ -150,7 +167,8 @@ def test_t1m_benchmark_calls_against_oracle():
     for name, (og, hg) in got.items():
         errs[name] = (assert_o(og, o_ref, BF16, f"{name} o"),
                       assert_s(hg, h_ref, BF16, f"{name} hT"))
-    print(f"\nT=2^20 H=32, heads {heads}: nseg {n_eff} (segment {sc} chunks, first {lead}x); "
+    print(f"\nT=2^20 H=32, heads {heads}: nseg {n_eff} (segment {sc} chunks, first {lead}x), "
+          f"decay-planned nseg {nseg_d} (first {lead_d}x); "
           + "; ".join(f"{n}: o {e[0]:.3e} hT {e[1]:.3e}" for n, e in errs.items()))
 
 
@@ -170,3 +188,76 @@ def test_short_workspace_is_rejected():
     with pytest.raises(kda.KdaError) as ei:
         run_seg(x, 2, workspace=ws)
     assert ei.value.code == kda.KDA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("B,T,H,dk,nsample", [
+    (2, 1000, 3, 128, 8),     # ragged last chunk
+    (1, 640, 2, 64, 40),      # more samples than chunks: chunks repeat
+    (3, 64, 1, 128, 1),
+    (1, 300, 19, 128, 5),     # heads over three CTAs, the last one partly idle
+])
+def test_decay_probe_matches_definition(B, T, H, dk, nsample):
+    """d_probe[b, s, h] = sum over the tokens of chunk floor(s * nch / nsample)
+    of max over channels of g[b, t, h]."""
+    gen = torch.Generator(device=DEV).manual_seed(B * 100 + T)
+    g = -5 * torch.sigmoid(torch.randn(B, T, H, dk, generator=gen, device=DEV))
+    got = kda.kda_chunk_fwd_decay_probe(g, nsample=nsample)
+    torch.cuda.synchronize()
+    gd = g.double().cpu()
+    nch = (T + 63) // 64
+    for b in range(B):
+        for s_ in range(nsample):
+            c = s_ * nch // nsample
+            want = gd[b, 64 * c:min(T, 64 * c + 64)].amax(dim=-1).sum(dim=0)  # [H]
+            err = (got[b, s_].double().cpu() - want).abs().max().item()
+            assert err <= 1e-5 * want.abs().max().item() + 1e-5, (b, s_, c)
+
+
+def test_hint_decay_plans():
+    """Strong decay (every run with v = 0 stops after a few chunks): more,
+    shorter segments and a shorter first one than the shape-only hint; no
+    decay information, or decay too weak to count on: the shape-only plan."""
+    B, T, H = 1, 1 << 20, 32
+    n0 = kda.kda_chunk_fwd_segments_hint(B, T, H, 128, 128)
+    _, sc0, lead0 = kda.kda_chunk_fwd_segment_plan(B, T, H, 128, 128, nseg=n0)
+    n, lead = kda.kda_chunk_fwd_segments_hint_decay(B, T, H, 128, 128, probe=[-20.0, -25.0])
+    _, sc, _ = kda.kda_chunk_fwd_segment_plan(B, T, H, 128, 128, nseg=n, lead=lead)
+    assert n > n0 and lead * sc < lead0 * sc0, (n, lead, sc, n0, lead0, sc0)
+    for weak in ([], [0.0], [-20.0, float("nan")], [-1e-3]):
+        n1, lead1 = kda.kda_chunk_fwd_segments_hint_decay(B, T, H, 128, 128, probe=weak)
+        _, _, lead_shape = kda.kda_chunk_fwd_segment_plan(B, T, H, 128, 128, nseg=n1)
+        assert n1 == n0 and lead1 == lead_shape, weak
+    # many sequences: no split, whatever the decay
+    assert kda.kda_chunk_fwd_segments_hint_decay(8, 8192, 32, 128, 128, probe=[-50.0]) == (1, 1)
+
+
+@pytest.mark.parametrize("nseg,lead", [(6, 2), (7, 3), (16, 4)])
+def test_explicit_lead_matches_oracle(nseg, lead):
+    """B=1, T=2000 (32 chunks, ragged), H=4: a first segment of `lead`
+    segment lengths, as kda_chunk_fwd_segment_plan reports it."""
+    T = 2000
+    n, sc, ld = kda.kda_chunk_fwd_segment_plan(1, T, 4, 128, 128, nseg=nseg, lead=lead)
+    assert ld == lead and (ld + n - 1) * sc >= 32 > (ld + n - 2) * sc
+    x = inputs.prefill_inputs(workload(True), DEV, B=1, T=T, H=4, seed=17 + nseg)
+    o, hT, st = run_seg(x, nseg, lead=lead)
+    assert st == 0
+    xc = {nm: (t.cpu() if t is not None else None) for nm, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, BF16)
+    assert_s(hT, h_ref, BF16)
+
+
+def test_decay_planned_call_matches_oracle():
+    """nseg="decay" on the T = 4096 stress workload (half the heads at
+    g = -4.99): probe, plan and segmented call, against the oracle."""
+    w = inputs.PREFILL_T4K
+    x = inputs.prefill_inputs(w, DEV)
+    o, hT = kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                        nseg="decay")
+    torch.cuda.synchronize()
+    heads = [0, 7, 16, 31]
+    sub = {n: x[n][:, :, heads].contiguous().cpu() for n in ("q", "k", "v", "g", "beta")}
+    h0 = x["h0"][:, heads].contiguous().cpu() if x["h0"] is not None else None
+    o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], h0)
+    assert_o(o[:, :, heads], o_ref, BF16)
+    assert_s(hT[:, heads], h_ref, BF16)
