@@ -3,14 +3,15 @@
     python -m gated_delta_rule_57_gb300.profile_cases prefill [--B 8] [--calls 4]
     python -m gated_delta_rule_57_gb300.profile_cases decode  [--calls 4]
     python -m gated_delta_rule_57_gb300.profile_cases spec    [--calls 4]
-    python -m gated_delta_rule_57_gb300.profile_cases long    [--T 65536] [--nseg 5] [--calls 4]
+    python -m gated_delta_rule_57_gb300.profile_cases long    [--T 65536] [--nseg 5|decay] [--calls 4]
 
 Draws the seeded synthetic inputs on the GPU, then makes `calls` back-to-back
 calls of kda_chunk_fwd (prefill: B x 8192 tokens x 32 heads, d = 128, bf16)
 or kda_decode_step (256 sequences x 32 heads, d = 128), or rounds of
 kda_decode_multi (the same 256 x 32 states, 4 draft tokens: verify then
 commit), or kda_chunk_fwd_segmented (long: one sequence of T tokens x 32 heads
-split into nseg segments; three launches per call). Under a profiler,
+split into nseg segments; three launches per call; --nseg decay plans the
+split from kda_chunk_fwd_decay_probe, one launch more). Under a profiler,
 skip the first calls as warm-up (e.g. ncu -s 2 -c 1 -k regex:kda_).
 """
 import argparse
@@ -25,7 +26,7 @@ def main():
     ap.add_argument("which", choices=["prefill", "decode", "spec", "long"])
     ap.add_argument("--B", type=int, default=8)
     ap.add_argument("--T", type=int, default=65536)
-    ap.add_argument("--nseg", type=int, default=5)
+    ap.add_argument("--nseg", default="5", help="segment count, or 'decay'")
     ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
     dev = torch.device("cuda", 0)
@@ -46,9 +47,13 @@ def main():
         x = inputs.prefill_inputs(w, dev, T=args.T)
         o = torch.empty_like(x["v"])
         hT = torch.empty(w.B, w.H, w.dk, w.dv, device=dev)
+        nseg = args.nseg if args.nseg == "decay" else int(args.nseg)
+        ws = torch.empty(kda.kda_chunk_fwd_segmented_workspace_size(
+            w.B, args.T, w.H, w.dk, w.dv, nseg=min(32, (args.T + 63) // 64)),
+            dtype=torch.uint8, device=dev)
         for _ in range(args.calls):
             kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
-                                        nseg=args.nseg, o=o, hT=hT)
+                                        nseg=nseg, o=o, hT=hT, workspace=ws)
     else:
         w = inputs.DECODE_N256
         x = inputs.prefill_inputs(inputs.PrefillWorkload("draft", w.N, 4, w.H, w.dk, w.dv, w.io,

@@ -261,3 +261,26 @@ def test_decay_planned_call_matches_oracle():
     o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], h0)
     assert_o(o[:, :, heads], o_ref, BF16)
     assert_s(hT[:, heads], h_ref, BF16)
+
+
+def test_slow_decay_runs_whole_segments():
+    """Decay near zero (g = -0.01 on every channel) over chunks 10..29 and
+    g = -4.99 elsewhere: the transition and correction runs of the slow
+    stretch cannot stop early and run their whole segments, the others stop
+    after a chunk or two. The probe tells the two apart (chunk 0 against
+    chunk 16); under plans with several segment lengths the results match
+    the oracle."""
+    B, T, H = 1, 2000, 4  # 32 chunks
+    x = inputs.prefill_inputs(workload(True), DEV, B=B, T=T, H=H, seed=31)
+    x["g"].fill_(-4.99)
+    x["g"][:, 640:1920] = -0.01  # chunks 10..29
+    probe = kda.kda_chunk_fwd_decay_probe(x["g"], nsample=2)  # chunks 0 and 16
+    torch.cuda.synchronize()
+    assert probe[0, 0].max().item() < -300 and probe[0, 1].max().item() > -1
+    for nseg, lead in ((8, 2), (6, 1)):
+        o, hT, st = run_seg(x, nseg, lead=lead)
+        assert st == 0
+        xc = {nm: (t.cpu() if t is not None else None) for nm, t in x.items()}
+        o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+        assert_o(o, o_ref, BF16, f"nseg {nseg} lead {lead}")
+        assert_s(hT, h_ref, BF16, f"nseg {nseg} lead {lead}")
