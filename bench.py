@@ -293,11 +293,12 @@ def time_prefill_e2e(xh, steps, warmup, device):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    # Three timed runs of `steps` pipelined steps each; the median run is the
-    # number (a host-side stall of the enqueueing thread, which the GPU then
-    # waits for, lands in one run, not in all three).
+    # Five timed runs of `steps` pipelined steps each; the median run is the
+    # number, and all five are reported (on a shared machine some runs of the
+    # pipelined step slow down for a while after heavy GPU work, while single
+    # large copies keep the link's rate).
     runs = []
-    for _ in range(3):
+    for _ in range(5):
         start.record(s_in)
         for _ in range(steps):
             step()
