@@ -414,10 +414,10 @@ def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
     """A workload with few sequences (B*H well below the SM count), timed in
     one pass (kda_chunk_fwd), split in time into the segment count
     kda_chunk_fwd_segments_hint picks (kda_chunk_fwd_segmented: segment
-    pass, scan, correction), and split as planned from the decay statistic
-    (kda_chunk_fwd_decay_probe, its B x 64 x H floats copied to the host,
-    kda_chunk_fwd_segments_hint_decay, then kda_chunk_fwd_segmented with that
-    nseg and lead: all of it inside each timed step). Each call is timed alone
+    pass, scan, correction), and split as planned on the device from the
+    decay statistic (kda_chunk_fwd_segmented with nseg = 0: the probe and
+    planning kernels, then the three passes reading the plan; all of it inside
+    each timed step, no host round trip). Each call is timed alone
     with CUDA events; with flush_l2 a 256 MB buffer is written before each
     timed call, so inputs that fit in part in L2 start cold. Returns
     (single-pass ms, segmented ms, nseg, launches per segmented call,
@@ -427,12 +427,10 @@ def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
     o = torch.empty_like(x["v"])
     hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=device)
     nseg = kda.kda_chunk_fwd_segments_hint(w.B, w.T, w.H, w.dk, w.dv)
-    nseg_max = min(32, (w.T + 63) // 64)
     ws = torch.empty(max(1, kda.kda_chunk_fwd_segmented_workspace_size(
-        w.B, w.T, w.H, w.dk, w.dv, nseg=nseg_max)), dtype=torch.uint8, device=device)
-    probe = torch.empty(w.B, 64, w.H, dtype=torch.float32, device=device)
-    probe_h = torch.empty(w.B, 64, w.H, dtype=torch.float32).pin_memory()
-    planned = [None]
+        w.B, w.T, w.H, w.dk, w.dv, nseg=nseg)), dtype=torch.uint8, device=device)
+    ws_plan = torch.empty(max(1, kda.kda_chunk_fwd_segmented_workspace_size(
+        w.B, w.T, w.H, w.dk, w.dv, nseg=0)), dtype=torch.uint8, device=device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if flush_l2 else None
     stream = torch.cuda.current_stream()
 
@@ -445,13 +443,8 @@ def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
                                     nseg=nseg, o=o, hT=hT, workspace=ws, stream=stream)
 
     def decay_planned():
-        kda.kda_chunk_fwd_decay_probe(x["g"], out=probe, stream=stream)
-        probe_h.copy_(probe, non_blocking=True)
-        stream.synchronize()
-        n, ld = kda.kda_chunk_fwd_segments_hint_decay(w.B, w.T, w.H, w.dk, w.dv, probe=probe_h)
-        planned[0] = (n, ld)
         kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
-                                    nseg=n, lead=ld, o=o, hT=hT, workspace=ws, stream=stream)
+                                    nseg=0, o=o, hT=hT, workspace=ws_plan, stream=stream)
 
     res = []
     for f in (single, segmented, decay_planned):
@@ -468,9 +461,12 @@ def time_single_and_segmented(w, device, seed, iters, warmup, flush_l2=False):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         res.append(statistics.mean(a.elapsed_time(b) for a, b in ev))
-    del x, o, ws, flush
+    # the plan the device chose, recomputed by the host's copy of the planner
+    planned = kda.kda_chunk_fwd_segments_hint_decay(
+        w.B, w.T, w.H, w.dk, w.dv, probe=kda.kda_chunk_fwd_decay_probe(x["g"]))
+    del x, o, ws, ws_plan, flush
     torch.cuda.empty_cache()
-    return res[0], res[1], nseg, (3 if nseg > 1 else 1), res[2], planned[0]
+    return res[0], res[1], nseg, (3 if nseg > 1 else 1), res[2], planned
 
 
 def few_sequences_obj(w, device, rank, world, peaks, iters, warmup, flush_l2):
@@ -495,9 +491,10 @@ def few_sequences_obj(w, device, rank, world, peaks, iters, warmup, flush_l2):
             "nseg": nd, "lead": ld, "ms_per_step": td, "value": job_value(tok, td, world),
             "unit": "tokens/s",
             "frac_of_peak_hbm": nbytes / (td * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "launches_per_step": 1 + (3 if nd > 1 else 1),
-            "what": "decay probe of g, its result read back on the host, plan, segmented "
-                    "call: all inside the timed step"},
+            "launches_per_step": 5,
+            "what": "kda_chunk_fwd_segmented with nseg = 0: decay probe of g and planning "
+                    "kernel, then the passes reading the plan, all inside the timed step; "
+                    "nseg and lead as the host's copy of the planner gives them"},
         "speedup": t1 / ts,
         "speedup_decay_planned": t1 / td,
         "algorithmic_bytes_per_step": nbytes,

@@ -10,6 +10,8 @@
 #include <mutex>
 
 #include "kda_internal.cuh"
+
+using kda::segment_shape;
 #include <nvtx3/nvToolsExt.h>
 
 namespace {
@@ -135,18 +137,6 @@ cudaError_t seg_scratch_address(void** out) {
 
 namespace {
 
-// Segments of a split sequence: segment 0 spans lead * sc chunks, every later
-// one sc = ceil(chunks / (lead + nseg - 1)); *nseg_eff is the number of
-// non-empty segments that gives (at most nseg).
-void segment_shape(int T, int nseg, int lead, int* seg_chunks, int* nseg_eff) {
-    const int nch = (T + 63) / 64;
-    const int sc = nch > 0 ? (nch + lead + nseg - 2) / (lead + nseg - 1) : 1;
-    *seg_chunks = sc;
-    int ne = 1;
-    while (ne < nseg && (long long)(lead + ne - 1) * sc < nch) ne++;
-    *nseg_eff = ne;
-}
-
 // SMs of the current device, 0 if none is visible.
 int device_sms() {
     int dev = 0, nsm = 0;
@@ -159,43 +149,17 @@ int device_sms() {
     return nsm;
 }
 
-// Chunk steps on the critical path of a split run with one CTA per SM. The
-// segment pass starts the BH long first segments, the other SMs take the
-// 2 BH (nseg - 1) short runs (segments from zero and transitions) and every
-// SM joins once the long runs end; the correction pass has BH (nseg - 1)
-// short runs. tl < 0: the runs with v = 0 (transitions, corrections) take
-// their whole segment; else about tl chunks (they stop once their state is
-// exactly zero). Returns -1 when the split leaves empty segments.
-long long split_cost(long long BH, int T, int nseg, int lead, int nsm, long long tl = -1) {
-    int sc, se;
-    segment_shape(T, nseg, lead, &sc, &se);
-    if (se != nseg) return -1;
-    auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
-    if (tl >= 0 && tl < sc) {
-        // The BH (nseg - 1) segments from zero run sc chunks each, the
-        // transitions (dispatched after them) and corrections about tl.
-        const long long z = BH * (nseg - 1);
-        long long p1;
-        if (BH >= nsm) {
-            p1 = waves(BH) * lead * sc + waves(z) * (sc + tl);
-        } else {
-            const long long free_sms = nsm - BH, wz = (z + free_sms - 1) / free_sms;
-            p1 = wz <= lead ? std::max((long long)lead * sc, wz * (sc + tl))
-                            : ((long long)lead + waves(z - free_sms * lead)) * sc + waves(z) * tl;
-        }
-        return p1 + waves(z) * tl;
-    }
-    const long long shorts = 2 * BH * (nseg - 1);
-    long long p1;
-    if (BH >= nsm) {
-        p1 = waves(BH) * lead * sc + waves(shorts) * sc;
-    } else {
-        const long long free_sms = nsm - BH;
-        const long long w = (shorts + free_sms - 1) / free_sms;
-        p1 = w <= lead ? (long long)lead * sc
-                       : ((long long)lead + waves(shorts - free_sms * lead)) * sc;
-    }
-    return p1 + waves(BH * (nseg - 1)) * sc;
+// Device-planned split (nseg = 0): plans of up to min(32, chunks) segments;
+// the workspace holds their states, then the decay probe (kPlanSamples chunks
+// per batch row and head), then the plan {nseg, seg_chunks, lead}.
+constexpr int kPlanSamples = 64;
+int planned_max_segments(int T) {
+    const int nch = (T + 63) / 64;
+    return nch < kda::kPlanMaxSeg ? nch : kda::kPlanMaxSeg;
+}
+size_t probe_floats(int B, int H) { return ((size_t)B * kPlanSamples * H + 3) & ~(size_t)3; }
+size_t planned_workspace_bytes(int B, int H, int nseg_max) {
+    return (kda::segmented_workspace_floats((long long)B * H, nseg_max) + probe_floats(B, H)) * 4 + 16;
 }
 
 // The first segment's length in short segments for a split into nseg on nsm
@@ -203,6 +167,7 @@ long long split_cost(long long BH, int T, int nseg, int lead, int nsm, long long
 // even split (so the workspace does not depend on the device); 1 without a
 // device (nsm = 0).
 int choose_lead(long long BH, int T, int nseg, int nsm, long long tl = -1) {
+    using kda::split_cost;
     if (nseg <= 1 || nsm <= 0) return 1;
     int best = 1;
     long long best_cost = split_cost(BH, T, nseg, 1, nsm, tl);
@@ -269,22 +234,32 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
     }
 
     int seg_chunks = 0, nseg_eff = 1, lead = 1;
+    int nseg_max = 0;  // a device-planned split (nseg = 0): the largest plan
     if (nseg != 1) {
         if (io != KDA_BF16 || dk != 128)
             return fail(KDA_ERR_UNSUPPORTED, "segmented prefill needs bf16 and dk = dv = 128");
         const int nch = (T + 63) / 64;
-        if (nseg < 1 || (T > 0 && nseg > nch))
+        if (nseg == 0) {
+            if (lead_in > 0)
+                return fail(KDA_ERR_INVALID_ARG, "a device-planned split (nseg = 0) takes no lead");
+            if (B > 65535) return fail(KDA_ERR_INVALID_ARG, "a device-planned split needs B <= 65535");
+            nseg_max = planned_max_segments(T);
+        } else if (nseg < 1 || (T > 0 && nseg > nch))
             return fail(KDA_ERR_INVALID_ARG, "nseg must be in 1 .. ceil(T / 64)");
         if (lead_in > 0 && T > 0 && lead_in > nch)
             return fail(KDA_ERR_INVALID_ARG, "lead must be <= 0 (the library's choice) or in 1 .. ceil(T / 64)");
-        segment_shape(T, nseg, 1, &seg_chunks, &nseg_eff);
-        lead = lead_in > 0 ? lead_in : choose_lead((long long)B * H, T, nseg_eff, device_sms());
-        segment_shape(T, nseg_eff, lead, &seg_chunks, &nseg_eff);
+        if (nseg > 0) {
+            segment_shape(T, nseg, 1, &seg_chunks, &nseg_eff);
+            lead = lead_in > 0 ? lead_in : choose_lead((long long)B * H, T, nseg_eff, device_sms());
+            segment_shape(T, nseg_eff, lead, &seg_chunks, &nseg_eff);
+        }
     }
     // Every argument but the workspace is valid.
     if (check_only) return KDA_OK;
-    if (nseg_eff > 1) {
-        const size_t need = kda::segmented_workspace_floats((long long)B * H, nseg_eff) * 4;
+    if (nseg_eff > 1 || nseg_max > 1) {
+        const size_t need = nseg_max > 1
+                                ? planned_workspace_bytes(B, H, nseg_max)
+                                : kda::segmented_workspace_floats((long long)B * H, nseg_eff) * 4;
         if (!workspace || ws_bytes < need)
             return fail(KDA_ERR_WORKSPACE, "workspace smaller than the segmented size");
         if (!aligned16(workspace))
@@ -319,11 +294,24 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
         }
         a.bal_ws = bal_ws;
     }
-    cudaError_t e = nseg_eff > 1
-                        ? kda::launch_chunk_fwd_tc_segmented(a, nseg_eff, seg_chunks, lead,
-                                                             static_cast<float*>(workspace))
-                    : io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
-                                     : kda::launch_chunk_fwd_simt(a, io);
+    cudaError_t e;
+    if (nseg_max > 1) {
+        // probe -> plan -> segment pass, scan, correction: all on the stream
+        const long long BH = (long long)B * H;
+        float* wsf = static_cast<float*>(workspace);
+        float* probe = wsf + kda::segmented_workspace_floats(BH, nseg_max);
+        int* plan = reinterpret_cast<int*>(probe + probe_floats(B, H));
+        e = kda::launch_decay_probe(g, B, T, H, dk, kPlanSamples, probe, a.stream);
+        if (e == cudaSuccess)
+            e = kda::launch_segment_plan(probe, B * kPlanSamples * H, BH, T, device_sms(),
+                                         nseg_max, plan, a.stream);
+        if (e == cudaSuccess) e = kda::launch_chunk_fwd_tc_segmented_planned(a, nseg_max, wsf, plan);
+    } else {
+        e = nseg_eff > 1 ? kda::launch_chunk_fwd_tc_segmented(a, nseg_eff, seg_chunks, lead,
+                                                              static_cast<float*>(workspace))
+            : io == KDA_BF16 ? kda::launch_chunk_fwd_tc(a)
+                             : kda::launch_chunk_fwd_simt(a, io);
+    }
     if (e != cudaSuccess) {
         set_last_error(cudaGetErrorString(e));
         return KDA_ERR_CUDA;
@@ -359,47 +347,25 @@ int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t
     if ((long long)B * H >= (1LL << 31)) return -1;
     if (io != KDA_BF16 || dk != 128 || B == 0 || H == 0) return 1;
     const int nsm = device_sms();
-    if (nsm == 0) return 1;
-    // Chunk steps on the critical path: whole sequences take ceil(BH / nsm)
-    // waves of nch chunks; a split costs split_cost with its best first
-    // segment length plus about one chunk step per scan step. More segments
-    // mean more scan steps and workspace: take a larger count only if it
-    // saves at least 2 %.
-    const long long BH = (long long)B * H, nch = (T + 63) / 64;
-    const long long base = ((BH + nsm - 1) / nsm) * nch;
-    int best = 1;
-    long long best_cost = -1;
-    for (int s = 2; s <= 32 && s <= nch; s++) {
-        int sc, se;
-        segment_shape(T, s, 1, &sc, &se);
-        if (se != s) continue;
-        const long long c = split_cost(BH, T, s, choose_lead(BH, T, s, nsm), nsm);
-        if (c < 0) continue;
-        const long long cost = c + (s - 1);
-        if (best_cost < 0 || cost * 50 < best_cost * 49) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    // Segments cost extra work (three passes over the split part) and HBM
-    // traffic; take them only for a clear gain.
-    return best_cost >= 0 && best_cost * 5 < base * 4 ? best : 1;
+    if (nsm <= 0) return 1;
+    const long long BH = (long long)B * H;
+    // Whole segments for every run: the data is not known here.
+    long long cost[kda::kPlanCosts];
+    kda::fill_plan_costs(BH, T, nsm, -1, cost);
+    return kda::choose_plan(BH, T, nsm, kda::kPlanMaxSeg, cost).nseg;
 }
 
 int kda_chunk_fwd_segments_hint_decay(int B, int T, int H, int dk, int dv, kda_dtype_t io,
-                                      const float* probe, int nprobe, int* lead) {
+                                                                        const float* probe, int nprobe, int* lead) {
     if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return -1;
     if ((long long)B * H >= (1LL << 31)) return -1;
     if (nprobe < 0 || (nprobe > 0 && !probe)) return -1;
     if (lead) *lead = 1;
     if (io != KDA_BF16 || dk != 128 || B == 0 || H == 0) return 1;
     const int nsm = device_sms();
-    if (nsm == 0) return 1;
-    // The weakest decay per chunk the sample shows; a run with v = 0 loses
-    // at least that much (log scale) per chunk, and is exactly zero once the
-    // total passes fp32's smallest subnormal (2^-149 = e^-103.28), one chunk
-    // later it has stopped. No sample, a non-negative or non-finite entry:
-    // count the runs as whole segments, as kda_chunk_fwd_segments_hint does.
+    if (nsm <= 0) return 1;
+    // The weakest decay per chunk the sample shows (no entries, or a
+    // non-finite one: unknown, so whole segments).
     float cd = nprobe > 0 ? -INFINITY : 0.f;
     for (int i = 0; i < nprobe; i++) {
         if (!std::isfinite(probe[i])) {
@@ -408,29 +374,12 @@ int kda_chunk_fwd_segments_hint_decay(int B, int T, int H, int dk, int dv, kda_d
         }
         cd = std::max(cd, probe[i]);
     }
-    const long long BH = (long long)B * H, nch = (T + 63) / 64;
-    long long tl = -1;
-    if (cd < 0.f) tl = std::min<long long>(nch, 2 + (long long)std::ceil(103.28f / -cd));
-    const long long base = ((BH + nsm - 1) / nsm) * nch;
-    int best = 1, best_lead = 1;
-    long long best_cost = -1;
-    for (int s = 2; s <= 32 && s <= nch; s++) {
-        int sc, se;
-        segment_shape(T, s, 1, &sc, &se);
-        if (se != s) continue;
-        const int ld = choose_lead(BH, T, s, nsm, tl);
-        const long long c = split_cost(BH, T, s, ld, nsm, tl);
-        if (c < 0) continue;
-        const long long cost = c + (s - 1);
-        if (best_cost < 0 || cost * 50 < best_cost * 49) {
-            best_cost = cost;
-            best = s;
-            best_lead = ld;
-        }
-    }
-    if (!(best_cost >= 0 && best_cost * 5 < base * 4)) return 1;
-    if (lead) *lead = best_lead;
-    return best;
+    const long long BH = (long long)B * H, tl = kda::transition_chunks(cd, T);
+    long long cost[kda::kPlanCosts];
+    kda::fill_plan_costs(BH, T, nsm, tl, cost);
+    const kda::SegPlan plan = kda::choose_plan(BH, T, nsm, kda::kPlanMaxSeg, cost);
+    if (lead) *lead = plan.lead;
+    return plan.nseg;
 }
 
 kda_status_t kda_chunk_fwd_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
@@ -483,8 +432,13 @@ size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int d
     if (B < 0 || T < 0 || H < 0 || check_dims(dk, dv, io) != KDA_OK) return (size_t)-1;
     if ((long long)B * H >= (1LL << 31)) return (size_t)-1;
     const int nch = (T + 63) / 64;
+    if (nseg != 1 && (io != KDA_BF16 || dk != 128)) return (size_t)-1;
+    if (nseg == 0) {  // planned on the device
+        if (B > 65535) return (size_t)-1;
+        const int nmax = planned_max_segments(T);
+        return nmax > 1 && B > 0 && H > 0 ? planned_workspace_bytes(B, H, nmax) : 0;
+    }
     if (nseg < 1 || (T > 0 && nseg > nch)) return (size_t)-1;
-    if (nseg > 1 && (io != KDA_BF16 || dk != 128)) return (size_t)-1;
     int sc, se;
     segment_shape(T, nseg, 1, &sc, &se);
     return se > 1 ? kda::segmented_workspace_floats((long long)B * H, se) * 4 : 0;

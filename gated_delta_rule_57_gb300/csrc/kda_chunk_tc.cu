@@ -142,6 +142,10 @@ struct TcParams {
     // v = 0 and writes the slice's transition to ws_m[bh]; pass 4 runs from
     // ws_sin[bh] with v = 0 and adds its outputs to o.
     int pass, nseg, seg_chunks, lead, BH;
+    // Device-planned split (passes 1 and 2): {nseg, seg_chunks, lead} are read
+    // from here instead of the fields above, and the CTAs past the plan's
+    // tasks leave at once (the grid is sized for the largest plan).
+    const int* plan;
     // Balanced schedule of the whole-sequence kernel (bal_W > 0): CTA i covers
     // chunk steps [i bal_W, (i + 1) bal_W) of the sequences laid end to end
     // (bal_W >= the chunks of one sequence); a sequence split between two CTAs
@@ -449,6 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, u = warp >> 2;
     const int lane = 32 * q + (tid & 31);
     const int T = p.T;
+    int nseg = p.nseg, seg_chunks = p.seg_chunks, lead = p.lead;
+    if (SEG && p.plan) {
+        nseg = __ldg(p.plan);
+        seg_chunks = __ldg(p.plan + 1);
+        lead = __ldg(p.plan + 2);
+        const long long ntasks = p.pass == 1 ? (long long)p.BH * (2 * nseg - 1)
+                                             : (long long)p.BH * (nseg - 1);
+        if ((long long)blockIdx.x >= ntasks) return;  // before any barrier or TMEM
+    }
     // This CTA's task (see TcParams): kind 0 runs a whole sequence or a segment
     // from h0 / zero writing o, kind 1 a segment from the identity with v = 0
     // (its transition), kind 2 a segment from its incoming state with v = 0,
@@ -457,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kind = !SEG                          ? 0
                      : p.pass == 3                 ? 1
                      : p.pass == 2 || p.pass == 4  ? 2
-                     : (p.pass == 1 && (int)blockIdx.x >= p.BH * p.nseg) ? 1
+                     : (p.pass == 1 && (int)blockIdx.x >= p.BH * nseg) ? 1
                                                                           : 0;
     const bool v_zero = kind != 0;
     const bool whole = !SEG || p.pass == 0 || p.pass >= 3;  // one CTA runs all the chunks
@@ -465,13 +478,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bh = blockIdx.x, seg = 0;
         if (whole) {
         } else if (kind == 2 || kind == 1) {
-            const int j = kind == 1 ? (int)blockIdx.x - p.BH * p.nseg : (int)blockIdx.x;
-            bh = j / (p.nseg - 1);
-            seg = 1 + j % (p.nseg - 1);
+            const int j = kind == 1 ? (int)blockIdx.x - p.BH * nseg : (int)blockIdx.x;
+            bh = j / (nseg - 1);
+            seg = 1 + j % (nseg - 1);
         } else if (SEG && p.pass == 1 && (int)blockIdx.x >= p.BH) {
             const int j = (int)blockIdx.x - p.BH;
-            bh = j / (p.nseg - 1);
-            seg = 1 + j % (p.nseg - 1);
+            bh = j / (nseg - 1);
+            seg = 1 + j % (nseg - 1);
         }
         *bh_out = bh;
         *seg_out = seg;
@@ -479,16 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bh, seg;
     task_seq(&bh, &seg);
     int b = bh / p.H, h = bh % p.H;
-    int t_begin = seg == 0 ? 0 : (p.lead + seg - 1) * p.seg_chunks * kC;
+    int t_begin = seg == 0 ? 0 : (lead + seg - 1) * seg_chunks * kC;
     // Initial state: h0 (whole sequences and first segments), zero (other
     // segments), the identity (transition runs) or the incoming state.
     const float* h0p = (kind == 2 && whole) ? p.ws_sin + (size_t)bh * kD * kD
-                       : kind == 2 ? p.ws_sin + ((size_t)bh * (p.nseg - 1) + seg - 1) * kD * kD
+                       : kind == 2 ? p.ws_sin + ((size_t)bh * (nseg - 1) + seg - 1) * kD * kD
                        : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * kD * kD
                                                          : nullptr;
     int nchunks = whole
                       ? (T + kC - 1) / kC
-                      : min(seg == 0 ? p.lead * p.seg_chunks : p.seg_chunks,
+                      : min(seg == 0 ? lead * seg_chunks : seg_chunks,
                             (T - t_begin + kC - 1) / kC);
     // Tasks of this CTA: one, except in the balanced schedule, where the range
     // [lo, hi) of chunk steps gives the head of sequence s_last (chunks
@@ -1231,8 +1244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * kD * kD : nullptr;
         else if (p.pass == 3) hTp = p.ws_m + (size_t)bh2 * kD * kD;
         else if (p.pass == 4) hTp = nullptr;
-        else if (kind == 0) hTp = p.ws_s0 + ((size_t)bh2 * p.nseg + seg2) * kD * kD;
-        else if (kind == 1) hTp = p.ws_m + ((size_t)bh2 * (p.nseg - 1) + seg2 - 1) * kD * kD;
+        else if (kind == 0) hTp = p.ws_s0 + ((size_t)bh2 * nseg + seg2) * kD * kD;
+        else if (kind == 1) hTp = p.ws_m + ((size_t)bh2 * (nseg - 1) + seg2 - 1) * kD * kD;
     }
     if (hTp && !failed) {
         float* dst = hTp + lane;
@@ -1323,6 +1336,7 @@ TcParams base_params(const ChunkFwdArgs& a) {
     p.bal_W = 0;
     p.bal_states = nullptr;
     p.bal_flags = nullptr;
+    p.plan = nullptr;
     return p;
 }
 
@@ -1434,6 +1448,32 @@ cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int s
     if (e != cudaSuccess) return e;
     p.pass = 2;
     return launch_tc<true>(m, p, BH * (nseg - 1), a.stream);
+}
+
+cudaError_t launch_chunk_fwd_tc_segmented_planned(const ChunkFwdArgs& a, int nseg_max,
+                                                  float* ws, const int* plan) {
+    TcMaps m;
+    if (!make_maps(&m, a)) return cudaErrorInvalidValue;
+    const long long BH = (long long)a.B * a.H;
+    const size_t DD = (size_t)kD * kD;
+    // Regions sized for nseg_max segments, indexed with the plan's count.
+    float* s0 = ws;
+    float* mt = s0 + (size_t)BH * nseg_max * DD;
+    float* sin = mt + (size_t)BH * (nseg_max - 1) * DD;
+    TcParams p = base_params(a);
+    p.nseg = nseg_max;
+    p.plan = plan;
+    p.ws_s0 = s0;
+    p.ws_m = mt;
+    p.ws_sin = sin;
+    p.hT = nullptr;  // the final state comes out of the scan
+    p.pass = 1;
+    cudaError_t e = launch_tc<true>(m, p, BH * (2 * nseg_max - 1), a.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_segment_scan_planned(s0, mt, sin, a.hT, (int)BH, plan, a.stream);
+    if (e != cudaSuccess) return e;
+    p.pass = 2;
+    return launch_tc<true>(m, p, BH * (nseg_max - 1), a.stream);
 }
 
 }  // namespace kda

@@ -81,6 +81,58 @@ __global__ void __launch_bounds__(32 * kProbeWarps)
     if (lane == 0) out[((size_t)b * nsample + s) * H + h] = sum;
 }
 
+// The split of a device-planned segmented prefill, from a decay probe: the
+// largest finite entry is cd (none, or a non-finite one: whole-segment runs,
+// as without a probe); the threads fill the cost table of every (segment
+// count, first-segment length), and one thread takes the same choice as the
+// host's kda_chunk_fwd_segments_hint_decay, writing {nseg, seg_chunks, lead}.
+constexpr int kPlanThreads = 512;
+
+__global__ void __launch_bounds__(kPlanThreads)
+    kda_segment_plan_kernel(const float* __restrict__ probe, int nprobe, long long BH, int T,
+                            int nsm, int nseg_max, int* __restrict__ plan) {
+    __shared__ float s_max[kPlanThreads / 32];
+    __shared__ int s_bad[kPlanThreads / 32];
+    __shared__ long long s_cost[kPlanCosts];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float m = -INFINITY;
+    int bad = 0;
+    for (int i = tid; i < nprobe; i += kPlanThreads) {
+        const float x = probe[i];
+        if (isfinite(x)) m = fmaxf(m, x);
+        else bad = 1;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        bad |= __shfl_xor_sync(0xffffffffu, bad, off);
+    }
+    if (lane == 0) {
+        s_max[warp] = m;
+        s_bad[warp] = bad;
+    }
+    __syncthreads();
+    float cd = -INFINITY;
+    int any_bad = 0;
+    for (int w = 0; w < kPlanThreads / 32; w++) {
+        cd = fmaxf(cd, s_max[w]);
+        any_bad |= s_bad[w];
+    }
+    if (nprobe == 0 || any_bad) cd = 0.f;
+    const long long tl = transition_chunks(cd, T);
+    for (int e = tid; e < kPlanCosts; e += kPlanThreads) {
+        const int sg = e / kPlanStride, l = e % kPlanStride;
+        s_cost[e] = (sg >= 2 && l >= 1 && nsm > 0) ? split_cost(BH, T, sg, l, nsm, tl) : -1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const SegPlan sp = choose_plan(BH, T, nsm, nseg_max, s_cost);
+        plan[0] = sp.nseg;
+        plan[1] = sp.seg_chunks;
+        plan[2] = sp.lead;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
@@ -90,6 +142,13 @@ cudaError_t launch_decay_probe(const float* g, int B, int T, int H, int dk, int 
         kda_decay_probe_kernel<128><<<grid, 32 * kProbeWarps, 0, stream>>>(g, T, H, nsample, out);
     else
         kda_decay_probe_kernel<64><<<grid, 32 * kProbeWarps, 0, stream>>>(g, T, H, nsample, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segment_plan(const float* probe, int nprobe, long long BH, int T, int nsm,
+                                int nseg_max, int* plan, cudaStream_t stream) {
+    kda_segment_plan_kernel<<<1, kPlanThreads, 0, stream>>>(probe, nprobe, BH, T, nsm, nseg_max,
+                                                            plan);
     return cudaGetLastError();
 }
 

@@ -70,6 +70,8 @@ cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int s
                                           int lead, float* ws);
 cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                                 int nseg, cudaStream_t stream);
+cudaError_t launch_segment_scan_planned(const float* s0, const float* m, float* sin, float* hT,
+                                        int BH, const int* plan, cudaStream_t stream);
 // One time slice of every sequence (bf16, dk = dv = 128), for a sequence
 // split across devices: which = 1 writes the slice's transition (the run
 // from the identity with v = 0) to state [B*H][dk][dk]; which = 2 runs from
@@ -96,6 +98,145 @@ inline size_t segmented_workspace_floats(long long BH, int nseg) {
     // nseg - 1 incoming states, 128 x 128 fp32 each
     return (size_t)BH * (size_t)(3 * nseg - 2) * 128u * 128u;
 }
+// ---- Planning a split in time (shared by the host hints and the planning
+// kernel, so both choose the same split).
+//
+// Segments of a sequence of nch = ceil(T / 64) chunks split into nseg:
+// segment 0 spans lead * sc chunks, every later one sc = ceil(nch / (lead +
+// nseg - 1)); *nseg_eff is the number of non-empty segments that gives (at
+// most nseg): the least count whose lengths reach nch.
+__host__ __device__ inline void segment_shape(int T, int nseg, int lead, int* seg_chunks,
+                                              int* nseg_eff) {
+    const int nch = (T + 63) / 64;
+    const int sc = nch > 0 ? (nch + lead + nseg - 2) / (lead + nseg - 1) : 1;
+    int ne = (nch + sc - 1) / sc - lead + 1;
+    ne = ne < 1 ? 1 : (ne > nseg ? nseg : ne);
+    *seg_chunks = sc;
+    *nseg_eff = ne;
+}
+
+// Chunk steps on the critical path of a split run with one CTA per SM. The
+// segment pass starts the BH long first segments, the other SMs take the
+// 2 BH (nseg - 1) short runs (segments from zero and transitions) and every
+// SM joins once the long runs end; the correction pass has BH (nseg - 1)
+// short runs. tl < 0: the runs with v = 0 (transitions, corrections) take
+// their whole segment; else about tl chunks (they stop once their state is
+// exactly zero). Returns -1 when the split leaves empty segments.
+__host__ __device__ inline long long split_cost(long long BH, int T, int nseg, int lead, int nsm,
+                                                long long tl = -1) {
+    int sc, se;
+    segment_shape(T, nseg, lead, &sc, &se);
+    if (se != nseg) return -1;
+    auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
+    if (tl >= 0 && tl < sc) {
+        // The BH (nseg - 1) segments from zero run sc chunks each, the
+        // transitions (dispatched after them) and corrections about tl.
+        const long long z = BH * (nseg - 1);
+        long long p1;
+        if (BH >= nsm) {
+            p1 = waves(BH) * lead * sc + waves(z) * (sc + tl);
+        } else {
+            const long long free_sms = nsm - BH, wz = (z + free_sms - 1) / free_sms;
+            const long long a = (long long)lead * sc, b = wz * (sc + tl);
+            p1 = wz <= lead ? (a > b ? a : b)
+                            : ((long long)lead + waves(z - free_sms * lead)) * sc + waves(z) * tl;
+        }
+        return p1 + waves(z) * tl;
+    }
+    const long long shorts = 2 * BH * (nseg - 1);
+    long long p1;
+    if (BH >= nsm) {
+        p1 = waves(BH) * lead * sc + waves(shorts) * sc;
+    } else {
+        const long long free_sms = nsm - BH;
+        const long long w = (shorts + free_sms - 1) / free_sms;
+        p1 = w <= lead ? (long long)lead * sc
+                       : ((long long)lead + waves(shorts - free_sms * lead)) * sc;
+    }
+    return p1 + waves(BH * (nseg - 1)) * sc;
+}
+
+constexpr int kPlanMaxSeg = 32;   // segment counts considered: 2 .. 32
+constexpr int kPlanMaxLead = 16;  // first-segment lengths considered: 1 .. 16
+
+// Transition length (chunks) to count on for a probe statistic cd (the
+// largest sum over a chunk of the per-token max log-decay; see
+// kda_chunk_fwd_decay_probe): a state shrinks at least by e^cd per chunk and
+// is exactly zero past 2^-149 = e^-103.28, one chunk later the run has
+// stopped. cd >= 0 or not finite: -1 (whole segments).
+__host__ __device__ inline long long transition_chunks(float cd, int T) {
+    if (!(cd < 0.f)) return -1;
+    const long long nch = (T + 63) / 64;
+    const long long t = 2 + (long long)ceilf(103.28f / -cd);
+    return t < nch ? t : nch;
+}
+
+// The plan: the segment count of 2 .. min(32, nch, nseg_max) with the fewest
+// chunk steps on the critical path (each at its best first-segment length of
+// 1 .. 16, plus one step per scan step), a larger count taken only when it
+// saves 2 %, and no split (1) unless it saves a fifth against whole
+// sequences. cost[s * kPlanStride + l] = split_cost for s segments and lead l
+// (filled for s = 2 .. 32, l = 1 .. 16; see fill_plan_costs).
+struct SegPlan {
+    int nseg, seg_chunks, lead;
+};
+constexpr int kPlanStride = kPlanMaxLead + 1;
+constexpr int kPlanCosts = (kPlanMaxSeg + 1) * kPlanStride;
+__host__ __device__ inline SegPlan choose_plan(long long BH, int T, int nsm, int nseg_max,
+                                               const long long* cost) {
+    const long long nch = (T + 63) / 64;
+    SegPlan plan{1, (int)(nch > 0 ? nch : 1), 1};
+    if (nsm <= 0 || BH <= 0 || nch < 2) return plan;
+    const long long base = ((BH + nsm - 1) / nsm) * nch;
+    int best = 1, best_lead = 1;
+    long long best_cost = -1;
+    for (int s = 2; s <= kPlanMaxSeg && s <= nch && s <= nseg_max; s++) {
+        int sc, se;
+        segment_shape(T, s, 1, &sc, &se);
+        if (se != s) continue;
+        int ld = 1;
+        long long c = cost[s * kPlanStride + 1];
+        if (c >= 0) {
+            for (int l = 2; l <= kPlanMaxLead; l++) {
+                const long long cl = cost[s * kPlanStride + l];
+                if (cl >= 0 && cl < c) {
+                    c = cl;
+                    ld = l;
+                }
+            }
+        }
+        if (c < 0) continue;
+        const long long total = c + (s - 1);
+        if (best_cost < 0 || total * 50 < best_cost * 49) {
+            best_cost = total;
+            best = s;
+            best_lead = ld;
+        }
+    }
+    if (!(best_cost >= 0 && best_cost * 5 < base * 4)) return plan;
+    plan.nseg = best;
+    plan.lead = best_lead;
+    int se;
+    segment_shape(T, best, best_lead, &plan.seg_chunks, &se);
+    return plan;
+}
+
+// Host side: the whole cost table, one entry at a time (nsm > 0).
+inline void fill_plan_costs(long long BH, int T, int nsm, long long tl, long long* cost) {
+    for (int s = 0; s <= kPlanMaxSeg; s++)
+        for (int l = 0; l <= kPlanMaxLead; l++)
+            cost[s * kPlanStride + l] = (s >= 2 && l >= 1) ? split_cost(BH, T, s, l, nsm, tl) : -1;
+}
+
+// Device-planned split (kda_chunk_fwd_segmented with nseg = 0): the planning
+// kernel reduces a decay probe to cd and writes {nseg, seg_chunks, lead} to
+// plan (device), which the segment pass, the scan and the correction pass
+// read; their grids are sized for nseg_max segments.
+cudaError_t launch_segment_plan(const float* probe, int nprobe, long long BH, int T, int nsm,
+                                int nseg_max, int* plan, cudaStream_t stream);
+cudaError_t launch_chunk_fwd_tc_segmented_planned(const ChunkFwdArgs& a, int nseg_max,
+                                                  float* ws, const int* plan);
+
 cudaError_t launch_decode(const DecodeArgs& a, kda_dtype_t io);
 cudaError_t launch_decode_multi(const MultiDecodeArgs& a, kda_dtype_t io);
 cudaError_t launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream);

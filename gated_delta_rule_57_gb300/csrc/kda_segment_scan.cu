@@ -55,10 +55,16 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// plan (device, nullable): a device-planned split, whose segment count
+// replaces nseg (segment-major layout).
 __global__ void __launch_bounds__(kScanThreads, 1)
     kda_segment_scan_kernel(const float* __restrict__ s0, const float* __restrict__ m,
                             float* __restrict__ sin, float* __restrict__ hT, int nseg,
-                            const ScanLayout L) {
+                            ScanLayout L, const int* __restrict__ plan) {
+    if (plan) {
+        nseg = __ldg(plan);
+        L = ScanLayout{1, nseg, 1, nseg - 1, 1, nseg - 1};
+    }
     extern __shared__ __align__(16) float smem[];
     float* Mb = smem;                      // [2][kDs][kLdm]   M of the current and next segment
     float* Sb = smem + 2 * kMFloats;       // [2][kDs][kCols]  their blocks of S0
@@ -154,13 +160,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 }  // namespace
 
 static cudaError_t launch_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
-                               int nseg, const ScanLayout& L, cudaStream_t stream) {
+                               int nseg, const ScanLayout& L, cudaStream_t stream,
+                               const int* plan = nullptr) {
     cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kScanSmem);
     if (e != cudaSuccess) return e;
     kda_segment_scan_kernel<<<dim3(BH, kColBlocks), kScanThreads, kScanSmem, stream>>>(
-        s0, m, sin, hT, nseg, L);
+        s0, m, sin, hT, nseg, L, plan);
     return cudaGetLastError();
 }
 
@@ -168,6 +175,12 @@ cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, flo
                                 int nseg, cudaStream_t stream) {
     const ScanLayout L{1, nseg, 1, nseg - 1, 1, nseg - 1};
     return launch_scan(s0, m, sin, hT, BH, nseg, L, stream);
+}
+
+cudaError_t launch_segment_scan_planned(const float* s0, const float* m, float* sin, float* hT,
+                                        int BH, const int* plan, cudaStream_t stream) {
+    const ScanLayout L{1, 1, 1, 1, 1, 1};  // replaced from the plan in the kernel
+    return launch_scan(s0, m, sin, hT, BH, 1, L, stream, plan);
 }
 
 cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,

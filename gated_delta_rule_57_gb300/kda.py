@@ -247,9 +247,10 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg=None,
                             status: Optional[torch.Tensor] = None, workspace=None, stream=None):
     """kda_chunk_fwd with each sequence split in time into `nseg` segments run
     in parallel, the first spanning `lead` segment lengths. nseg None: the
-    library's shape-only hint for this device; nseg "decay": plan with
-    kda_chunk_fwd_decay_probe of g (a host round trip that waits for the
-    probe). lead None: the library's choice for nseg. Returns (o, hT)."""
+    library's shape-only hint for this device; nseg "decay" (or 0): planned
+    on the device from kda_chunk_fwd_decay_probe's statistic of g (no host
+    round trip; lead must be None). lead None: the library's choice for
+    nseg. Returns (o, hT)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     io = _DTYPE.get(q.dtype)
@@ -258,11 +259,7 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, h0=None, *, nseg=None,
     if nseg is None:
         nseg = kda_chunk_fwd_segments_hint(B, T, H, dk, dv, q.dtype)
     elif nseg == "decay":
-        probe = kda_chunk_fwd_decay_probe(g, stream=stream)
-        with torch.cuda.stream(stream):  # the copy waits for the probe on its stream
-            host = probe.to("cpu")
-        nseg, ld = kda_chunk_fwd_segments_hint_decay(B, T, H, dk, dv, q.dtype, host)
-        lead = ld if lead is None else lead
+        nseg = 0
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_hT:

@@ -174,7 +174,14 @@ kda_status_t kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, con
  * (o of later segments is the sum of two bf16-rounded parts).
  *
  *   nseg      : segments per sequence, 1 .. ceil(T / 64); 1 runs
- *               kda_chunk_fwd. As many segments result as an even split into
+ *               kda_chunk_fwd. 0: planned on the device from the data:
+ *               kda_chunk_fwd_decay_probe's statistic of g is reduced by a
+ *               planning kernel to the split kda_chunk_fwd_segments_hint_decay
+ *               would choose (up to min(32, ceil(T / 64)) segments), and the
+ *               passes read it from device memory; five launches, no host
+ *               synchronisation (so it can be captured into a CUDA graph); B
+ *               must be <= 65535 and lead <= 0; with fewer than two chunks
+ *               it runs kda_chunk_fwd. As many segments result as an even split into
  *               ceil(ceil(T / 64) / nseg)-chunk segments leaves non-empty
  *               (at most nseg); the first, which needs no transition and no
  *               correction, may span several segment lengths so that its long
@@ -206,7 +213,10 @@ kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v
 /*
  * Bytes of workspace kda_chunk_fwd_segmented needs: (3 nseg' - 2) * dk * dv * 4
  * per (b, h), nseg' the number of segments that results, 0 when that is 1.
- * Returns (size_t)-1 for arguments kda_chunk_fwd_segmented would reject.
+ * For nseg = 0 (planned on the device): the same for nseg' = min(32,
+ * ceil(T / 64)), plus 64 * B * H floats of probe (rounded up to 16 bytes) and
+ * 16 bytes of plan (0 with fewer than two chunks). Returns (size_t)-1 for
+ * arguments kda_chunk_fwd_segmented would reject.
  */
 size_t kda_chunk_fwd_segmented_workspace_size(int B, int T, int H, int dk, int dv,
                                               kda_dtype_t io, int nseg);
@@ -300,7 +310,8 @@ int kda_chunk_fwd_segments_hint_decay(int B, int T, int H, int dk, int dv, kda_d
  * The split kda_chunk_fwd_segmented uses for nseg and lead_in (its lead
  * argument; <= 0: the library's choice) on the current device: returns the
  * number of segments that results (1 = no split), or -1 for arguments
- * kda_chunk_fwd_segmented would reject. *seg_chunks (if not NULL)
+ * kda_chunk_fwd_segmented would reject and for nseg = 0 (that split is
+ * chosen on the device from the data). *seg_chunks (if not NULL)
  * receives the length of every segment after the first in 64-token chunks
  * (the last may be shorter; ceil(T / 64) when there is no split) and *lead
  * (if not NULL) the first segment's length in those units. The first segment

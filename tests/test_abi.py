@@ -168,7 +168,13 @@ def test_segmented_workspace_size(L):
     assert f(1, 1000, 2, 128, 128, kda.KDA_BF16, 7) == 2 * 16 * per    # 16 chunks -> 6 x 3
     assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 1) == 0
     assert f(1, 64, 1, 128, 128, kda.KDA_BF16, 1) == 0
-    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 0) == sz
+    # nseg = 0 (planned on the device): states for min(32, chunks) segments, then
+    # 64 x B x H probe floats (16-byte multiple) and a 16-byte plan
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 0) == 32 * 94 * per + 64 * 32 * 4 + 16
+    assert f(3, 1000, 1, 128, 128, kda.KDA_BF16, 0) == 3 * 46 * per + 192 * 4 + 16  # 16 chunks
+    assert f(1, 65, 5, 128, 128, kda.KDA_BF16, 0) == 5 * 4 * per + 320 * 4 + 16      # 2 chunks
+    assert f(1, 64, 5, 128, 128, kda.KDA_BF16, 0) == 0   # one chunk: no split
+    assert f(1, 4096, 32, 128, 128, kda.KDA_F32, 0) == sz
     assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 65) == sz             # more segments than chunks
     assert f(1, 4096, 32, 128, 128, kda.KDA_F32, 2) == sz               # no segmented fp32 path
     assert f(1, 4096, 32, 64, 64, kda.KDA_BF16, 2) == sz
@@ -216,6 +222,7 @@ def test_segment_plan(L):
     assert plan(1, 4096, 32, 16, lead_in=4) == 13 and (lead.value, sc.value) == (4, 4)
     assert plan(1, 4096, 32, 2, lead_in=64) == 1  # the first segment covers everything
     assert plan(1, 4096, 32, 2, lead_in=65) == -1  # longer than the sequence
+    assert plan(1, 4096, 32, 0) == -1  # planned on the device
 
 
 def test_segments_hint_decay(L):
@@ -267,7 +274,6 @@ def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(nseg=0), ST.KDA_ERR_INVALID_ARG),
     (dict(nseg=3), ST.KDA_ERR_INVALID_ARG),                       # 2 chunks
     (dict(io=kda.KDA_F32), ST.KDA_ERR_UNSUPPORTED),
     (dict(dk=64), ST.KDA_ERR_UNSUPPORTED),
@@ -277,6 +283,9 @@ def call_seg(L, nseg=2, ws=None, ws_bytes=0, T=128, dk=128, io=kda.KDA_BF16, q=A
     (dict(ws=A[0], ws_bytes=1 << 22), ST.KDA_ERR_INVALID_ARG),    # overlaps q
     (dict(q=None), ST.KDA_ERR_INVALID_ARG),
     (dict(lead=3), ST.KDA_ERR_INVALID_ARG),                       # longer than the 2 chunks
+    (dict(nseg=0, lead=1), ST.KDA_ERR_INVALID_ARG),               # a device plan takes no lead
+    (dict(nseg=0, ws=None, ws_bytes=0), ST.KDA_ERR_WORKSPACE),
+    (dict(nseg=-1), ST.KDA_ERR_INVALID_ARG),
 ])
 def test_segmented_rejects(L, kw, code):
     assert call_seg(L, **kw) == code

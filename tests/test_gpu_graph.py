@@ -121,3 +121,22 @@ def test_speculative_round_replays_bit_identical():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o_g, o_e) and torch.equal(S_g, S_e)
+
+
+def test_device_planned_split_replays_bit_identical():
+    """nseg = 0: probe, planning kernel and the three passes, all captured."""
+    B, T, H = 1, 4096, 8
+    w = inputs.PrefillWorkload("graph", B, T, H, 128, 128, "bf16", 45, h0_std=0.02)
+    x = inputs.prefill_inputs(w, DEV)
+    ws = torch.empty(kda.kda_chunk_fwd_segmented_workspace_size(B, T, H, 128, 128, nseg=0),
+                     dtype=torch.uint8, device=DEV)
+    o_e, h_e = kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                           nseg=0, workspace=ws)
+    o_g, h_g = torch.empty_like(o_e), torch.empty_like(h_e)
+    g = capture(lambda: kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                                    x["h0"], nseg=0, o=o_g, hT=h_g,
+                                                    workspace=ws))
+    o_g.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_g, o_e) and torch.equal(h_g, h_e)

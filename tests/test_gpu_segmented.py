@@ -111,8 +111,8 @@ def test_t1m_benchmark_calls_against_oracle():
     through the three calls the benchmark times: kda_chunk_fwd in one pass,
     kda_chunk_fwd_segmented with the segment count of
     kda_chunk_fwd_segments_hint and the library's first-segment length, and
-    kda_chunk_fwd_segmented planned from kda_chunk_fwd_decay_probe (more,
-    shorter segments, in a workspace sized for 32). The
+    kda_chunk_fwd_segmented planned on the device from the decay probe
+    (nseg = 0: more, shorter segments). The
     oracle recomputes four heads (two of them apart by half the head range)
     over the whole sequence, and every output and the final state of those
     heads is checked for both calls, so the transitions built over the long
@@ -145,7 +145,7 @@ def test_t1m_benchmark_calls_against_oracle():
     got["segmented"] = (o[:, :, heads].cpu(), hT[:, heads].cpu())
     del ws
     ws = torch.empty(kda.kda_chunk_fwd_segmented_workspace_size(w.B, w.T, w.H, w.dk, w.dv,
-                                                                nseg=32),
+                                                                nseg=0),
                      dtype=torch.uint8, device=DEV)
     probe = kda.kda_chunk_fwd_decay_probe(x["g"])
     nseg_d, lead_d = kda.kda_chunk_fwd_segments_hint_decay(w.B, w.T, w.H, w.dk, w.dv,
@@ -284,3 +284,29 @@ def test_slow_decay_runs_whole_segments():
         o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
         assert_o(o, o_ref, BF16, f"nseg {nseg} lead {lead}")
         assert_s(hT, h_ref, BF16, f"nseg {nseg} lead {lead}")
+
+
+@pytest.mark.parametrize("B,T,H,stress", [(1, 4096, 32, True), (2, 3000, 5, False),
+                                          (1, 900, 3, False)])
+def test_device_plan_equals_host_plan(B, T, H, stress):
+    """nseg = 0 (probe, planning kernel, passes reading the plan) gives exactly
+    the bits of the explicit split the host's copy of the planner picks from
+    the same probe, and matches the oracle."""
+    w = inputs.PrefillWorkload("plan", B, T, H, 128, 128, "bf16", 50 + T, h0_std=0.02,
+                               stress_heads=stress)
+    x = inputs.prefill_inputs(w, DEV)
+    o_d, h_d, st = run_seg(x, 0)
+    assert st == 0
+    n, lead = kda.kda_chunk_fwd_segments_hint_decay(B, T, H, 128, 128,
+                                                    probe=kda.kda_chunk_fwd_decay_probe(x["g"]))
+    if n > 1:
+        o_h, h_h, _ = run_seg(x, n, lead=lead)
+    else:
+        o_h, h_h = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+        torch.cuda.synchronize()
+    if n > 1:
+        assert torch.equal(o_d, o_h) and torch.equal(h_d, h_h), (n, lead)
+    xc = {nm: (t.cpu() if t is not None else None) for nm, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o_d, o_ref, BF16)
+    assert_s(h_d, h_ref, BF16)
