@@ -11,7 +11,7 @@ or kda_decode_step (256 sequences x 32 heads, d = 128), or rounds of
 kda_decode_multi (the same 256 x 32 states, 4 draft tokens: verify then
 commit), or kda_chunk_fwd_segmented (long: one sequence of T tokens x 32 heads
 split into nseg segments; three launches per call; --nseg decay plans the
-split from kda_chunk_fwd_decay_probe, one launch more). Under a profiler,
+split on the device from the decay probe: five launches). Under a profiler,
 skip the first calls as warm-up (e.g. ncu -s 2 -c 1 -k regex:kda_).
 """
 import argparse
@@ -47,10 +47,9 @@ def main():
         x = inputs.prefill_inputs(w, dev, T=args.T)
         o = torch.empty_like(x["v"])
         hT = torch.empty(w.B, w.H, w.dk, w.dv, device=dev)
-        nseg = args.nseg if args.nseg == "decay" else int(args.nseg)
+        nseg = 0 if args.nseg == "decay" else int(args.nseg)  # 0: planned on the device
         ws = torch.empty(kda.kda_chunk_fwd_segmented_workspace_size(
-            w.B, args.T, w.H, w.dk, w.dv, nseg=min(32, (args.T + 63) // 64)),
-            dtype=torch.uint8, device=dev)
+            w.B, args.T, w.H, w.dk, w.dv, nseg=nseg), dtype=torch.uint8, device=dev)
         for _ in range(args.calls):
             kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                         nseg=nseg, o=o, hT=hT, workspace=ws)
