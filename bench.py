@@ -293,20 +293,6 @@ def time_prefill_e2e(xh, steps, warmup, device):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    # Five timed runs of `steps` pipelined steps each; the median run is the
-    # number, and all five are reported (on a shared machine some runs of the
-    # pipelined step slow down for a while after heavy GPU work, while single
-    # large copies keep the link's rate).
-    runs = []
-    for _ in range(5):
-        start.record(s_in)
-        for _ in range(steps):
-            step()
-        end.record(s_out)
-        torch.cuda.synchronize()
-        runs.append(start.elapsed_time(end) / steps)
-    e2e_ms = statistics.median(runs)
-
     # The host link alone: the step's input bytes up as one copy from one
     # pinned buffer and its output bytes down as one copy into another, at
     # the same time on two streams, nothing else. Copy engines and SM loads of
@@ -318,27 +304,39 @@ def time_prefill_e2e(xh, steps, warmup, device):
     db_out = torch.empty(d2h, dtype=torch.uint8, device=device)
 
     def link():
-        with torch.cuda.stream(s_in):
-            db_in.copy_(hb_in, non_blocking=True)
-        with torch.cuda.stream(s_out):
-            hb_out.copy_(db_out, non_blocking=True)
-
-    link()
-    torch.cuda.synchronize()
-    link_ms = []
-    for _ in range(steps):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t2 = torch.cuda.Event(enable_timing=True)
         t0.record(s_in)
         s_out.wait_event(t0)
-        link()
+        with torch.cuda.stream(s_in):
+            db_in.copy_(hb_in, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hb_out.copy_(db_out, non_blocking=True)
         t1.record(s_in)
         t2.record(s_out)
         torch.cuda.synchronize()
-        link_ms.append(max(t0.elapsed_time(t1), t0.elapsed_time(t2)))
+        return max(t0.elapsed_time(t1), t0.elapsed_time(t2))
+
+    link()
+    # Nine timed runs of `steps` pipelined steps, each right after one timing
+    # of the link alone. The median run is the number; every run and its link
+    # time are reported, and the link fraction is the median of the per-run
+    # ratios. (On a shared machine the host link itself slows down in bursts
+    # of some hundred milliseconds after heavy GPU work: a run in a burst is
+    # slow, and so is the link timed beside it.)
+    runs, links = [], []
+    for _ in range(9):
+        links.append(link())
+        start.record(s_in)
+        for _ in range(steps):
+            step()
+        end.record(s_out)
+        torch.cuda.synchronize()
+        runs.append(start.elapsed_time(end) / steps)
+    e2e_ms = statistics.median(runs)
     del hb_in, db_in, hb_out, db_out
-    return e2e_ms, statistics.median(link_ms), h2d, d2h, o_h, hT_h, runs
+    return e2e_ms, links, h2d, d2h, o_h, hT_h, runs
 
 
 def time_decode(device, seed, warmup=10):
@@ -550,8 +548,10 @@ def run_ours(args):
 
     # end to end through the same call, pinned host buffers, copies timed
     xh = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "h0")}
-    e2e_ms, link_ms, h2d, d2h, o_host, hT_host, e2e_runs = time_prefill_e2e(
-        xh, max(3, min(args.steps, 20)), 2, device)
+    e2e_ms, e2e_links, h2d, d2h, o_host, hT_host, e2e_runs = time_prefill_e2e(
+        xh, max(3, min(args.steps, 10)), 2, device)
+    link_ms = statistics.median(e2e_links)
+    link_frac = statistics.median(l / r for l, r in zip(e2e_links, e2e_runs))
     # the pipelined host round trip must reproduce the device-resident result exactly
     e2e_exact = bool(torch.equal(o_host, o_dev.cpu()) and torch.equal(hT_host, hT_dev.cpu()))
     link_ms = max_over_ranks(link_ms, world, device)
@@ -628,11 +628,13 @@ def run_ours(args):
                     "matches_device_result": e2e_exact,
                     "host_link": {"ms_per_step": link_ms,
                                   "gbs_up": h2d / (link_ms * 1e-3) / 1e9,
-                                  "frac": link_ms / e2e_ms,
+                                  "frac": link_frac,
+                                  "runs_ms": e2e_links,
                                   "what": "the step's input bytes up as one copy and its "
                                           "output bytes down as another, concurrently, nothing "
-                                          "else: the floor of any step that moves them; frac = "
-                                          "that time / the e2e step"}},
+                                          "else: the floor of any step that moves them, timed "
+                                          "before each e2e run; frac = median over the runs of "
+                                          "that time / the run's step time"}},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "decode": {"workload": DECODE.name, "value": dec_gbs, "unit": "GB/s",
