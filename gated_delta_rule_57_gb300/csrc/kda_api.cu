@@ -152,7 +152,7 @@ int device_sms() {
 // Device-planned split (nseg = 0): plans of up to min(32, chunks) segments;
 // the workspace holds their states, then the decay probe (kPlanSamples chunks
 // per batch row and head), then the plan {nseg, seg_chunks, lead}.
-constexpr int kPlanSamples = 64;
+constexpr int kPlanSamples = 16;
 int planned_max_segments(int T) {
     const int nch = (T + 63) / 64;
     return nch < kda::kPlanMaxSeg ? nch : kda::kPlanMaxSeg;

@@ -14,39 +14,42 @@
 // floor(s * nch / nsample) of batch row b (a short last chunk sums its tokens
 // only). The planner takes the largest entry as the decay per chunk that the
 // sequences can be counted on; it is an estimate from a sample, so it guides
-// the plan only: results never depend on it. One warp per (sample, row,
-// head) reads the chunk's rows of that head (dk contiguous floats each) 16 at
-// a time, so that many loads are in flight per lane.
+// the plan only: results never depend on it. A CTA takes one sample of one
+// batch row for eight heads; four warps per head read 16 of the chunk's rows
+// each (dk contiguous floats per row), all loads in flight before any is used,
+// and the four partial sums are added in token order.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kProbeWarps = 8;
-constexpr int kProbeRows = 16;  // rows of g in flight per warp
+constexpr int kProbeHeads = 8;   // heads per CTA
+constexpr int kProbeParts = 4;   // warps per head, 16 tokens each
+constexpr int kProbeRows = 16;   // rows of g in flight per warp
 
 template <int DK>
-__global__ void __launch_bounds__(32 * kProbeWarps)
+__global__ void __launch_bounds__(32 * kProbeHeads * kProbeParts)
     kda_decay_probe_kernel(const float* __restrict__ g, int T, int H, int nsample,
                            float* __restrict__ out) {
     constexpr int PER = DK / 32;  // floats per lane of a row: 4 or 2
+    __shared__ float s_part[kProbeHeads][kProbeParts];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = blockIdx.x, b = blockIdx.y, h = blockIdx.z * kProbeWarps + warp;
-    if (h >= H) return;
+    const int hl = warp / kProbeParts, part = warp % kProbeParts;
+    const int s = blockIdx.x, b = blockIdx.y, h = blockIdx.z * kProbeHeads + hl;
     const int nch = (T + 63) / 64;
     const int c = (int)(((long long)s * nch) / nsample);
-    const int t0 = c * 64, t1 = min(T, t0 + 64);
-    const float* base = g + (((size_t)b * T) * H + h) * DK + PER * lane;
-    const size_t row_stride = (size_t)H * DK;  // next token, same head
+    const int t0 = c * 64 + part * kProbeRows, t1 = min(T, c * 64 + 64);
     float sum = 0.f;
-    if (t1 - t0 == 64) {  // a whole chunk: the loads of a group go out before any is used
-        for (int t = t0; t < t1; t += kProbeRows) {
-            float m[kProbeRows];
+    if (h < H && t0 < t1) {
+        const float* base = g + (((size_t)b * T) * H + h) * DK + PER * lane;
+        const size_t row_stride = (size_t)H * DK;  // next token, same head
+        float m[kProbeRows];
+        if (t0 + kProbeRows <= t1) {  // a whole group: every load out before any use
             if constexpr (PER == 4) {
                 float4 f[kProbeRows];
 #pragma unroll
                 for (int u = 0; u < kProbeRows; u++)
-                    f[u] = __ldcs(reinterpret_cast<const float4*>(base + (size_t)(t + u) * row_stride));
+                    f[u] = __ldcs(reinterpret_cast<const float4*>(base + (size_t)(t0 + u) * row_stride));
 #pragma unroll
                 for (int u = 0; u < kProbeRows; u++)
                     m[u] = fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w));
@@ -54,38 +57,53 @@ __global__ void __launch_bounds__(32 * kProbeWarps)
                 float2 f[kProbeRows];
 #pragma unroll
                 for (int u = 0; u < kProbeRows; u++)
-                    f[u] = __ldcs(reinterpret_cast<const float2*>(base + (size_t)(t + u) * row_stride));
+                    f[u] = __ldcs(reinterpret_cast<const float2*>(base + (size_t)(t0 + u) * row_stride));
 #pragma unroll
                 for (int u = 0; u < kProbeRows; u++) m[u] = fmaxf(f[u].x, f[u].y);
             }
+        } else {  // the short last chunk
 #pragma unroll
             for (int u = 0; u < kProbeRows; u++) {
+                m[u] = -INFINITY;
+                if (t0 + u < t1) {
+                    const float* r = base + (size_t)(t0 + u) * row_stride;
+                    m[u] = r[0];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], off));
+                    for (int e = 1; e < PER; e++) m[u] = fmaxf(m[u], r[e]);
+                }
             }
-#pragma unroll
-            for (int u = 0; u < kProbeRows; u++) sum += m[u];
         }
-    } else {  // the short last chunk
-        for (int t = t0; t < t1; t++) {
-            const float* r = base + (size_t)t * row_stride;
-            float m = r[0];
 #pragma unroll
-            for (int e = 1; e < PER; e++) m = fmaxf(m, r[e]);
+        for (int u = 0; u < kProbeRows; u++) {
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            sum += m;
+            for (int off = 16; off > 0; off >>= 1)
+                m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], off));
+        }
+#pragma unroll
+        for (int u = 0; u < kProbeRows; u++)
+            if (t0 + u < t1) sum += m[u];
+    }
+    if (lane == 0) s_part[hl][part] = sum;
+    __syncthreads();
+    if (threadIdx.x < kProbeHeads) {
+        const int hh = blockIdx.z * kProbeHeads + threadIdx.x;
+        if (hh < H) {
+            float tot = 0.f;
+#pragma unroll
+            for (int p = 0; p < kProbeParts; p++) tot += s_part[threadIdx.x][p];  // token order
+            out[((size_t)b * nsample + s) * H + hh] = tot;
         }
     }
-    if (lane == 0) out[((size_t)b * nsample + s) * H + h] = sum;
 }
 
 // The split of a device-planned segmented prefill, from a decay probe: the
 // largest finite entry is cd (none, or a non-finite one: whole-segment runs,
-// as without a probe); the threads fill the cost table of every (segment
-// count, first-segment length), and one thread takes the same choice as the
-// host's kda_chunk_fwd_segments_hint_decay, writing {nseg, seg_chunks, lead}.
+// as without a probe). Warp w takes the segment counts 2 + w and 18 + w, its
+// lanes the first-segment lengths 1 .. 16, and reduces them to the count's
+// best (cost, lead); one thread then takes the same choice over the counts as
+// the host's kda_chunk_fwd_segments_hint_decay and writes {nseg, seg_chunks,
+// lead}. Costs use 32-bit arithmetic when every value fits (the same
+// numbers), else 64-bit.
 constexpr int kPlanThreads = 512;
 
 __global__ void __launch_bounds__(kPlanThreads)
@@ -93,7 +111,8 @@ __global__ void __launch_bounds__(kPlanThreads)
                             int nsm, int nseg_max, int* __restrict__ plan) {
     __shared__ float s_max[kPlanThreads / 32];
     __shared__ int s_bad[kPlanThreads / 32];
-    __shared__ long long s_cost[kPlanCosts];
+    __shared__ long long s_bc[kPlanMaxSeg + 1];
+    __shared__ int s_bl[kPlanMaxSeg + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float m = -INFINITY;
     int bad = 0;
@@ -120,13 +139,36 @@ __global__ void __launch_bounds__(kPlanThreads)
     }
     if (nprobe == 0 || any_bad) cd = 0.f;
     const long long tl = transition_chunks(cd, T);
-    for (int e = tid; e < kPlanCosts; e += kPlanThreads) {
-        const int sg = e / kPlanStride, l = e % kPlanStride;
-        s_cost[e] = (sg >= 2 && l >= 1 && nsm > 0) ? split_cost(BH, T, sg, l, nsm, tl) : -1;
+    const bool fits = plan_fits_32(BH, T, nsm);
+    const int l = lane + 1;
+    for (int k = 0; k < 2; k++) {
+        const int sg = 2 + warp + 16 * k;
+        long long c = -1;
+        if (sg <= kPlanMaxSeg && l <= kPlanMaxLead && nsm > 0)
+            c = fits ? (long long)split_cost_t<int>((int)BH, T, sg, l, nsm, (int)tl)
+                     : split_cost(BH, T, sg, l, nsm, tl);
+        // lead 1 decides whether the count is usable; then the least cost,
+        // the smallest lead among equal ones
+        const long long c1 = __shfl_sync(0xffffffffu, c, 0);
+        long long bc = c >= 0 ? c : 0x7fffffffffffffffLL;
+        int bl = l;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const long long oc = __shfl_xor_sync(0xffffffffu, bc, off);
+            const int ol = __shfl_xor_sync(0xffffffffu, bl, off);
+            if (oc < bc || (oc == bc && ol < bl)) {
+                bc = oc;
+                bl = ol;
+            }
+        }
+        if (lane == 0 && sg <= kPlanMaxSeg) {
+            s_bc[sg] = c1 < 0 ? c1 : bc;
+            s_bl[sg] = c1 < 0 ? 1 : bl;
+        }
     }
     __syncthreads();
     if (tid == 0) {
-        const SegPlan sp = choose_plan(BH, T, nsm, nseg_max, s_cost);
+        const SegPlan sp = choose_plan_best(BH, T, nsm, nseg_max, s_bc, s_bl);
         plan[0] = sp.nseg;
         plan[1] = sp.seg_chunks;
         plan[2] = sp.lead;
@@ -137,11 +179,12 @@ __global__ void __launch_bounds__(kPlanThreads)
 
 cudaError_t launch_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
                                float* out, cudaStream_t stream) {
-    const dim3 grid((unsigned)nsample, (unsigned)B, (unsigned)((H + kProbeWarps - 1) / kProbeWarps));
+    const dim3 grid((unsigned)nsample, (unsigned)B, (unsigned)((H + kProbeHeads - 1) / kProbeHeads));
+    constexpr int threads = 32 * kProbeHeads * kProbeParts;
     if (dk == 128)
-        kda_decay_probe_kernel<128><<<grid, 32 * kProbeWarps, 0, stream>>>(g, T, H, nsample, out);
+        kda_decay_probe_kernel<128><<<grid, threads, 0, stream>>>(g, T, H, nsample, out);
     else
-        kda_decay_probe_kernel<64><<<grid, 32 * kProbeWarps, 0, stream>>>(g, T, H, nsample, out);
+        kda_decay_probe_kernel<64><<<grid, threads, 0, stream>>>(g, T, H, nsample, out);
     return cudaGetLastError();
 }
 

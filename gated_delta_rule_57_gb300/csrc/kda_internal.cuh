@@ -100,6 +100,8 @@ inline size_t segmented_workspace_floats(long long BH, int nseg) {
 }
 // ---- Planning a split in time (shared by the host hints and the planning
 // kernel, so both choose the same split).
+constexpr int kPlanMaxSeg = 32;   // segment counts considered: 2 .. 32
+constexpr int kPlanMaxLead = 16;  // first-segment lengths considered: 1 .. 16
 //
 // Segments of a sequence of nch = ceil(T / 64) chunks split into nseg:
 // segment 0 spans lead * sc chunks, every later one sc = ceil(nch / (lead +
@@ -122,42 +124,53 @@ __host__ __device__ inline void segment_shape(int T, int nseg, int lead, int* se
 // short runs. tl < 0: the runs with v = 0 (transitions, corrections) take
 // their whole segment; else about tl chunks (they stop once their state is
 // exactly zero). Returns -1 when the split leaves empty segments.
-__host__ __device__ inline long long split_cost(long long BH, int T, int nseg, int lead, int nsm,
-                                                long long tl = -1) {
+template <typename I>
+__host__ __device__ inline I split_cost_t(I BH, int T, int nseg, int lead, int nsm, I tl) {
     int sc, se;
     segment_shape(T, nseg, lead, &sc, &se);
     if (se != nseg) return -1;
-    auto waves = [&](long long ctas) { return (ctas + nsm - 1) / nsm; };
+    const I n = nsm;
+    auto waves = [&](I ctas) { return (ctas + n - 1) / n; };
     if (tl >= 0 && tl < sc) {
         // The BH (nseg - 1) segments from zero run sc chunks each, the
         // transitions (dispatched after them) and corrections about tl.
-        const long long z = BH * (nseg - 1);
-        long long p1;
-        if (BH >= nsm) {
+        const I z = BH * (nseg - 1);
+        I p1;
+        if (BH >= n) {
             p1 = waves(BH) * lead * sc + waves(z) * (sc + tl);
         } else {
-            const long long free_sms = nsm - BH, wz = (z + free_sms - 1) / free_sms;
-            const long long a = (long long)lead * sc, b = wz * (sc + tl);
+            const I free_sms = n - BH, wz = (z + free_sms - 1) / free_sms;
+            const I a = (I)lead * sc, b = wz * (sc + tl);
             p1 = wz <= lead ? (a > b ? a : b)
-                            : ((long long)lead + waves(z - free_sms * lead)) * sc + waves(z) * tl;
+                            : ((I)lead + waves(z - free_sms * lead)) * sc + waves(z) * tl;
         }
         return p1 + waves(z) * tl;
     }
-    const long long shorts = 2 * BH * (nseg - 1);
-    long long p1;
-    if (BH >= nsm) {
+    const I shorts = 2 * BH * (nseg - 1);
+    I p1;
+    if (BH >= n) {
         p1 = waves(BH) * lead * sc + waves(shorts) * sc;
     } else {
-        const long long free_sms = nsm - BH;
-        const long long w = (shorts + free_sms - 1) / free_sms;
-        p1 = w <= lead ? (long long)lead * sc
-                       : ((long long)lead + waves(shorts - free_sms * lead)) * sc;
+        const I free_sms = n - BH;
+        const I w = (shorts + free_sms - 1) / free_sms;
+        p1 = w <= lead ? (I)lead * sc : ((I)lead + waves(shorts - free_sms * lead)) * sc;
     }
     return p1 + waves(BH * (nseg - 1)) * sc;
 }
+__host__ __device__ inline long long split_cost(long long BH, int T, int nseg, int lead, int nsm,
+                                                long long tl = -1) {
+    return split_cost_t<long long>(BH, T, nseg, lead, nsm, tl);
+}
+// True when every value split_cost forms for these sizes (s <= 32 segments,
+// leads <= 16, tl <= chunks) fits in 32 bits, so split_cost_t<int> gives the
+// same costs.
+__host__ __device__ inline bool plan_fits_32(long long BH, int T, int nsm) {
+    const long long nch = (T + 63) / 64;
+    if (nsm <= 0 || BH >= (1LL << 24) || nch >= (1LL << 24)) return false;
+    const long long waves_max = (BH * 2 * kPlanMaxSeg + nsm - 1) / nsm + kPlanMaxLead + 2;
+    return waves_max * (2 * nch + 2) * 4 < (1LL << 31);
+}
 
-constexpr int kPlanMaxSeg = 32;   // segment counts considered: 2 .. 32
-constexpr int kPlanMaxLead = 16;  // first-segment lengths considered: 1 .. 16
 
 // Transition length (chunks) to count on for a probe statistic cd (the
 // largest sum over a chunk of the per-token max log-decay; see
@@ -182,8 +195,26 @@ struct SegPlan {
 };
 constexpr int kPlanStride = kPlanMaxLead + 1;
 constexpr int kPlanCosts = (kPlanMaxSeg + 1) * kPlanStride;
-__host__ __device__ inline SegPlan choose_plan(long long BH, int T, int nsm, int nseg_max,
-                                               const long long* cost) {
+// For s segments: the cheapest first-segment length (the first of equal
+// costs), from row[l] = cost with lead l; -1 when lead 1 leaves empty segments.
+__host__ __device__ inline void best_lead(const long long* row, long long* cost, int* lead) {
+    int ld = 1;
+    long long c = row[1];
+    if (c >= 0) {
+        for (int l = 2; l <= kPlanMaxLead; l++) {
+            if (row[l] >= 0 && row[l] < c) {
+                c = row[l];
+                ld = l;
+            }
+        }
+    }
+    *cost = c;
+    *lead = ld;
+}
+// The choice over segment counts from each count's best (cost, lead):
+// bc[s], bl[s] for s = 2 .. 32.
+__host__ __device__ inline SegPlan choose_plan_best(long long BH, int T, int nsm, int nseg_max,
+                                                    const long long* bc, const int* bl) {
     const long long nch = (T + 63) / 64;
     SegPlan plan{1, (int)(nch > 0 ? nch : 1), 1};
     if (nsm <= 0 || BH <= 0 || nch < 2) return plan;
@@ -191,20 +222,9 @@ __host__ __device__ inline SegPlan choose_plan(long long BH, int T, int nsm, int
     int best = 1, best_lead = 1;
     long long best_cost = -1;
     for (int s = 2; s <= kPlanMaxSeg && s <= nch && s <= nseg_max; s++) {
-        int sc, se;
-        segment_shape(T, s, 1, &sc, &se);
-        if (se != s) continue;
-        int ld = 1;
-        long long c = cost[s * kPlanStride + 1];
-        if (c >= 0) {
-            for (int l = 2; l <= kPlanMaxLead; l++) {
-                const long long cl = cost[s * kPlanStride + l];
-                if (cl >= 0 && cl < c) {
-                    c = cl;
-                    ld = l;
-                }
-            }
-        }
+        // (a count whose even split leaves empty segments costs -1 at lead 1)
+        const int ld = bl[s];
+        const long long c = bc[s];
         if (c < 0) continue;
         const long long total = c + (s - 1);
         if (best_cost < 0 || total * 50 < best_cost * 49) {
@@ -219,6 +239,14 @@ __host__ __device__ inline SegPlan choose_plan(long long BH, int T, int nsm, int
     int se;
     segment_shape(T, best, best_lead, &plan.seg_chunks, &se);
     return plan;
+}
+// The same from the whole cost table (cost[s * kPlanStride + l]).
+__host__ __device__ inline SegPlan choose_plan(long long BH, int T, int nsm, int nseg_max,
+                                               const long long* cost) {
+    long long bc[kPlanMaxSeg + 1];
+    int bl[kPlanMaxSeg + 1];
+    for (int s = 0; s <= kPlanMaxSeg; s++) best_lead(cost + s * kPlanStride, &bc[s], &bl[s]);
+    return choose_plan_best(BH, T, nsm, nseg_max, bc, bl);
 }
 
 // Host side: the whole cost table, one entry at a time (nsm > 0).

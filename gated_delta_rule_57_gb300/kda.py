@@ -188,10 +188,12 @@ def kda_chunk_fwd_segments_hint(B: int, T: int, H: int, dk: int, dv: int,
     return int(n)
 
 
-def kda_chunk_fwd_decay_probe(g, nsample: int = 64, out=None, stream=None):
+def kda_chunk_fwd_decay_probe(g, nsample: int = 16, out=None, stream=None):
     """Sampled decay statistic of g [B,T,H,dk] for kda_chunk_fwd_segments_hint_decay:
     a [B, nsample, H] fp32 device tensor (per head, the sum over a sampled
-    chunk's tokens of the max over channels of g)."""
+    chunk's tokens of the max over channels of g). The default sample is the
+    one kda_chunk_fwd_segmented with nseg = 0 takes on the device, so the host
+    planner then picks the same split."""
     B, T, H, dk = g.shape
     if out is None:
         out = torch.empty((B, nsample, H), dtype=torch.float32, device=g.device)

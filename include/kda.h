@@ -214,7 +214,7 @@ kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v
  * Bytes of workspace kda_chunk_fwd_segmented needs: (3 nseg' - 2) * dk * dv * 4
  * per (b, h), nseg' the number of segments that results, 0 when that is 1.
  * For nseg = 0 (planned on the device): the same for nseg' = min(32,
- * ceil(T / 64)), plus 64 * B * H floats of probe (rounded up to 16 bytes) and
+ * ceil(T / 64)), plus 16 * B * H floats of probe (rounded up to 16 bytes) and
  * 16 bytes of plan (0 with fewer than two chunks). Returns (size_t)-1 for
  * arguments kda_chunk_fwd_segmented would reject.
  */
@@ -279,8 +279,8 @@ int kda_chunk_fwd_segments_hint(int B, int T, int H, int dk, int dv, kda_dtype_t
  *   nsample  : chunks sampled per batch row, 1 .. 4096
  *   d_probe  : device, B * nsample * H floats, 4-byte aligned, not
  *              overlapping g
- * One launch of B * nsample * ceil(H / 8) CTAs on `stream`, one warp per
- * (sample, row, head) reading that head's 64 rows of dk floats; nothing
+ * One launch of B * nsample * ceil(H / 8) CTAs on `stream`, four warps per
+ * (sample, row, head) reading 16 of that head's 64 rows of dk floats each; nothing
  * written when B, H or T is 0. dk must be 64 or 128 (KDA_ERR_UNSUPPORTED),
  * B <= 65535, H <= 524280. The statistic guides the plan only: the results
  * of the segmented call never depend on it.

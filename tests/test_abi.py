@@ -169,10 +169,10 @@ def test_segmented_workspace_size(L):
     assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 1) == 0
     assert f(1, 64, 1, 128, 128, kda.KDA_BF16, 1) == 0
     # nseg = 0 (planned on the device): states for min(32, chunks) segments, then
-    # 64 x B x H probe floats (16-byte multiple) and a 16-byte plan
-    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 0) == 32 * 94 * per + 64 * 32 * 4 + 16
-    assert f(3, 1000, 1, 128, 128, kda.KDA_BF16, 0) == 3 * 46 * per + 192 * 4 + 16  # 16 chunks
-    assert f(1, 65, 5, 128, 128, kda.KDA_BF16, 0) == 5 * 4 * per + 320 * 4 + 16      # 2 chunks
+    # 16 x B x H probe floats (16-byte multiple) and a 16-byte plan
+    assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 0) == 32 * 94 * per + 16 * 32 * 4 + 16
+    assert f(3, 1000, 1, 128, 128, kda.KDA_BF16, 0) == 3 * 46 * per + 48 * 4 + 16   # 16 chunks
+    assert f(1, 65, 5, 128, 128, kda.KDA_BF16, 0) == 5 * 4 * per + 80 * 4 + 16      # 2 chunks
     assert f(1, 64, 5, 128, 128, kda.KDA_BF16, 0) == 0   # one chunk: no split
     assert f(1, 4096, 32, 128, 128, kda.KDA_F32, 0) == sz
     assert f(1, 4096, 32, 128, 128, kda.KDA_BF16, 65) == sz             # more segments than chunks
