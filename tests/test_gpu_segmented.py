@@ -310,3 +310,19 @@ def test_device_plan_equals_host_plan(B, T, H, stress):
     o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
     assert_o(o_d, o_ref, BF16)
     assert_s(h_d, h_ref, BF16)
+
+
+@pytest.mark.parametrize("bad,flag", [(float("nan"), "KDA_DEV_NONFINITE"),
+                                      (0.5, "KDA_DEV_DECAY_RANGE")])
+def test_device_plan_with_bad_decay(bad, flag):
+    """A NaN or a positive log-decay in g: the device-planned split still runs
+    (a non-finite statistic makes the planner count whole-segment runs) and
+    the status word reports the value."""
+    B, T, H = 1, 2000, 4
+    x = inputs.prefill_inputs(workload(True), DEV, B=B, T=T, H=H, seed=70)
+    x["g"][0, 5, 2, 17] = bad  # inside chunk 0, which the probe samples
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], nseg=0,
+                                status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & getattr(kda, flag)
