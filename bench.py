@@ -625,6 +625,9 @@ def run_ours(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "pipelined_by_batch_row": True,
                     "runs_ms_per_step": e2e_runs,
+                    "best_run_ms_per_step": min(e2e_runs),
+                    "runs_slower_than_best_by_10pct": sum(r > 1.1 * min(e2e_runs)
+                                                          for r in e2e_runs),
                     "matches_device_result": e2e_exact,
                     "host_link": {"ms_per_step": link_ms,
                                   "gbs_up": h2d / (link_ms * 1e-3) / 1e9,
