@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(D, 384 / D)
 // 32-column value slice, lane (rg, cg) rows rg D/4 .. + D/4 - 1, columns
 // 4 cg .. + 3 of the slice.
 template <typename TIn, int D, int KMAX>
-__global__ void __launch_bounds__(D, KMAX <= 4 ? 5 : 3)
+__global__ void __launch_bounds__(D, KMAX <= 4 ? 6 : 3)
     kda_verify_block_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                             const TIn* __restrict__ v, const float* __restrict__ g,
                             const float* __restrict__ beta, const float* __restrict__ S,
