@@ -453,6 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, u = warp >> 2;
     const int lane = 32 * q + (tid & 31);
     const int T = p.T;
+    // Segment and correction passes may be launched as programmatic dependents
+    // of the kernel before them: nothing is read before that kernel is done.
+    if (SEG) asm volatile("griddepcontrol.wait;" ::: "memory");
     int nseg = p.nseg, seg_chunks = p.seg_chunks, lead = p.lead;
     if (SEG && p.plan) {
         nseg = __ldg(p.plan);
@@ -1340,14 +1343,30 @@ TcParams base_params(const ChunkFwdArgs& a) {
     return p;
 }
 
+// dependent: launch as a programmatic dependent of the stream's previous
+// kernel (its launch overlaps that kernel's end; the kernel waits for it).
 template <bool SEG>
-cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaStream_t stream) {
+cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaStream_t stream,
+                      bool dependent = false) {
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel<SEG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kda_chunk_tc_kernel<SEG><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.g, m.o,
-                                                                                 p);
-    return cudaGetLastError();
+    if (!dependent) {
+        kda_chunk_tc_kernel<SEG><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(
+            m.q, m.k, m.v, m.g, m.o, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_chunk_tc_kernel<SEG>, m.q, m.k, m.v, m.g, m.o, p);
 }
 
 }  // namespace
@@ -1447,7 +1466,7 @@ cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int s
     e = launch_segment_scan(s0, mt, sin, a.hT, (int)BH, nseg, a.stream);
     if (e != cudaSuccess) return e;
     p.pass = 2;
-    return launch_tc<true>(m, p, BH * (nseg - 1), a.stream);
+    return launch_tc<true>(m, p, BH * (nseg - 1), a.stream, true);
 }
 
 cudaError_t launch_chunk_fwd_tc_segmented_planned(const ChunkFwdArgs& a, int nseg_max,
@@ -1468,12 +1487,12 @@ cudaError_t launch_chunk_fwd_tc_segmented_planned(const ChunkFwdArgs& a, int nse
     p.ws_sin = sin;
     p.hT = nullptr;  // the final state comes out of the scan
     p.pass = 1;
-    cudaError_t e = launch_tc<true>(m, p, BH * (2 * nseg_max - 1), a.stream);
+    cudaError_t e = launch_tc<true>(m, p, BH * (2 * nseg_max - 1), a.stream, true);
     if (e != cudaSuccess) return e;
     e = launch_segment_scan_planned(s0, mt, sin, a.hT, (int)BH, plan, a.stream);
     if (e != cudaSuccess) return e;
     p.pass = 2;
-    return launch_tc<true>(m, p, BH * (nseg_max - 1), a.stream);
+    return launch_tc<true>(m, p, BH * (nseg_max - 1), a.stream, true);
 }
 
 }  // namespace kda

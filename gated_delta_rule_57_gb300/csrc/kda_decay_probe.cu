@@ -109,6 +109,8 @@ constexpr int kPlanThreads = 512;
 __global__ void __launch_bounds__(kPlanThreads)
     kda_segment_plan_kernel(const float* __restrict__ probe, int nprobe, long long BH, int T,
                             int nsm, int nseg_max, int* __restrict__ plan) {
+    // Launched as a programmatic dependent of the probe: wait for it first.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float s_max[kPlanThreads / 32];
     __shared__ int s_bad[kPlanThreads / 32];
     __shared__ long long s_bc[kPlanMaxSeg + 1];
@@ -190,9 +192,17 @@ cudaError_t launch_decay_probe(const float* g, int B, int T, int H, int dk, int 
 
 cudaError_t launch_segment_plan(const float* probe, int nprobe, long long BH, int T, int nsm,
                                 int nseg_max, int* plan, cudaStream_t stream) {
-    kda_segment_plan_kernel<<<1, kPlanThreads, 0, stream>>>(probe, nprobe, BH, T, nsm, nseg_max,
-                                                            plan);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_segment_plan_kernel, probe, nprobe, BH, T, nsm, nseg_max,
+                              plan);
 }
 
 }  // namespace kda

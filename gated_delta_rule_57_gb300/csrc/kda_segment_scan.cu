@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     kda_segment_scan_kernel(const float* __restrict__ s0, const float* __restrict__ m,
                             float* __restrict__ sin, float* __restrict__ hT, int nseg,
                             ScanLayout L, const int* __restrict__ plan) {
+    // Scans of a time split run as programmatic dependents of the segment
+    // pass: nothing is read before it is done (a no-op for other launches).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (plan) {
         nseg = __ldg(plan);
         L = ScanLayout{1, nseg, 1, nseg - 1, 1, nseg - 1};
@@ -159,28 +162,43 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
 }  // namespace
 
+// dependent: launched as a programmatic dependent of the stream's previous
+// kernel (the scan waits for it before reading anything).
 static cudaError_t launch_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                                int nseg, const ScanLayout& L, cudaStream_t stream,
-                               const int* plan = nullptr) {
+                               const int* plan = nullptr, bool dependent = false) {
     cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kScanSmem);
     if (e != cudaSuccess) return e;
-    kda_segment_scan_kernel<<<dim3(BH, kColBlocks), kScanThreads, kScanSmem, stream>>>(
-        s0, m, sin, hT, nseg, L, plan);
-    return cudaGetLastError();
+    if (!dependent) {
+        kda_segment_scan_kernel<<<dim3(BH, kColBlocks), kScanThreads, kScanSmem, stream>>>(
+            s0, m, sin, hT, nseg, L, plan);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH, kColBlocks);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.dynamicSmemBytes = kScanSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_segment_scan_kernel, s0, m, sin, hT, nseg, L, plan);
 }
 
 cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                                 int nseg, cudaStream_t stream) {
     const ScanLayout L{1, nseg, 1, nseg - 1, 1, nseg - 1};
-    return launch_scan(s0, m, sin, hT, BH, nseg, L, stream);
+    return launch_scan(s0, m, sin, hT, BH, nseg, L, stream, nullptr, true);
 }
 
 cudaError_t launch_segment_scan_planned(const float* s0, const float* m, float* sin, float* hT,
                                         int BH, const int* plan, cudaStream_t stream) {
     const ScanLayout L{1, 1, 1, 1, 1, 1};  // replaced from the plan in the kernel
-    return launch_scan(s0, m, sin, hT, BH, 1, L, stream, plan);
+    return launch_scan(s0, m, sin, hT, BH, 1, L, stream, plan, true);
 }
 
 cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
