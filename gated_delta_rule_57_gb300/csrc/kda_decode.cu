@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     __shared__ float s_red[2][RG][DVS];
     __shared__ float s_kq[NW];
 
+    pdl_wait();  // the previous step (or whatever came before) is done
     const int tid = threadIdx.x;
     constexpr int NS = DV / DVS;
     const size_t head = blockIdx.x / NS;  // n * H + h
@@ -135,10 +136,11 @@ template <typename TIn, int D>
 cudaError_t launch_t(const DecodeArgs& a) {
     constexpr int DVS = D / 2, NT = D;  // two CTAs per head, 16 rows x 4 columns per thread
     const unsigned grid = (unsigned)((long long)a.N * a.H * (D / DVS));
-    kda_decode_kernel<TIn, D, D, DVS, NT><<<grid, NT, 0, a.stream>>>(
-        static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
-        static_cast<const TIn*>(a.v), a.g, a.beta, a.S, static_cast<TIn*>(a.o), a.d_status);
-    return cudaGetLastError();
+    // a step of a decode loop: its launch overlaps the end of the previous one
+    return launch_dependent(kda_decode_kernel<TIn, D, D, DVS, NT>, dim3(grid), dim3(NT), 0,
+                            a.stream, static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
+                            static_cast<const TIn*>(a.v), a.g, a.beta, a.S,
+                            static_cast<TIn*>(a.o), a.d_status);
 }
 
 }  // namespace

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(D, 384 / D)
     __shared__ __align__(16) float s_v[kStage][D];
     __shared__ float s_kqp[kStage][NW], s_beta[kStage];
 
+    pdl_wait();  // the kernel before it in the stream is done
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t head = blockIdx.x;  // n * H + h
     const int n = (int)(head / H), hh = (int)(head % H);
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(D, KMAX <= 4 ? 6 : 3)
     __shared__ __align__(16) float s_v[KMAX][D];
     __shared__ float s_a[KMAX][KMAX], s_p[KMAX][KMAX], s_tp[KMAX][KMAX], s_beta[KMAX];
 
+    pdl_wait();  // the kernel before it in the stream is done
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t head = blockIdx.x;  // n * H + h
     const int n = (int)(head / H), hh = (int)(head % H);
@@ -414,16 +416,17 @@ cudaError_t launch_t(const MultiDecodeArgs& a) {
     const unsigned grid = (unsigned)((long long)a.N * a.H);
     if (!a.commit && a.o && a.K <= 8) {  // a verify of up to eight drafts: block form, state streamed
         auto vk = a.K <= 4 ? kda_verify_block_kernel<TIn, D, 4> : kda_verify_block_kernel<TIn, D, 8>;
-        vk<<<grid, D, 0, a.stream>>>(static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
-                                     static_cast<const TIn*>(a.v), a.g, a.beta, a.S,
-                                     static_cast<TIn*>(a.o), a.ntok, a.K, a.H, a.d_status);
-        return cudaGetLastError();
+        return launch_dependent(vk, dim3(grid), dim3(D), 0, a.stream,
+                                static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
+                                static_cast<const TIn*>(a.v), a.g, a.beta,
+                                static_cast<const float*>(a.S), static_cast<TIn*>(a.o), a.ntok,
+                                a.K, a.H, a.d_status);
     }
     auto kern = a.o ? kda_decode_multi_kernel<TIn, D, true> : kda_decode_multi_kernel<TIn, D, false>;
-    kern<<<grid, D, 0, a.stream>>>(static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k),
-                                   static_cast<const TIn*>(a.v), a.g, a.beta, a.S,
-                                   static_cast<TIn*>(a.o), a.ntok, a.K, a.H, a.commit, a.d_status);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(D), 0, a.stream, static_cast<const TIn*>(a.q),
+                            static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v), a.g,
+                            a.beta, a.S, static_cast<TIn*>(a.o), a.ntok, a.K, a.H, a.commit,
+                            a.d_status);
 }
 
 }  // namespace
