@@ -458,9 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (SEG) asm volatile("griddepcontrol.wait;" ::: "memory");
     int nseg = p.nseg, seg_chunks = p.seg_chunks, lead = p.lead;
     if (SEG && p.plan) {
-        nseg = __ldg(p.plan);
-        seg_chunks = __ldg(p.plan + 1);
-        lead = __ldg(p.plan + 2);
+        // clamped to the grid and workspace this launch was sized for
+        nseg = min(max(__ldg(p.plan), 1), p.nseg);
+        seg_chunks = max(__ldg(p.plan + 1), 1);
+        lead = max(__ldg(p.plan + 2), 1);
         const long long ntasks = p.pass == 1 ? (long long)p.BH * (2 * nseg - 1)
                                              : (long long)p.BH * (nseg - 1);
         if ((long long)blockIdx.x >= ntasks) return;  // before any barrier or TMEM
@@ -1489,7 +1490,7 @@ cudaError_t launch_chunk_fwd_tc_segmented_planned(const ChunkFwdArgs& a, int nse
     p.pass = 1;
     cudaError_t e = launch_tc<true>(m, p, BH * (2 * nseg_max - 1), a.stream, true);
     if (e != cudaSuccess) return e;
-    e = launch_segment_scan_planned(s0, mt, sin, a.hT, (int)BH, plan, a.stream);
+    e = launch_segment_scan_planned(s0, mt, sin, a.hT, (int)BH, nseg_max, plan, a.stream);
     if (e != cudaSuccess) return e;
     p.pass = 2;
     return launch_tc<true>(m, p, BH * (nseg_max - 1), a.stream, true);

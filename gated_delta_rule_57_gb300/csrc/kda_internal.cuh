@@ -71,7 +71,8 @@ cudaError_t launch_chunk_fwd_tc_segmented(const ChunkFwdArgs& a, int nseg, int s
 cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
                                 int nseg, cudaStream_t stream);
 cudaError_t launch_segment_scan_planned(const float* s0, const float* m, float* sin, float* hT,
-                                        int BH, const int* plan, cudaStream_t stream);
+                                        int BH, int nseg_max, const int* plan,
+                                        cudaStream_t stream);
 // One time slice of every sequence (bf16, dk = dv = 128), for a sequence
 // split across devices: which = 1 writes the slice's transition (the run
 // from the identity with v = 0) to state [B*H][dk][dk]; which = 2 runs from

@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // Scans of a time split run as programmatic dependents of the segment
     // pass: nothing is read before it is done (a no-op for other launches).
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (plan) {
-        nseg = __ldg(plan);
+    if (plan) {  // nseg is the largest plan the workspace holds
+        nseg = min(max(__ldg(plan), 1), nseg);
         L = ScanLayout{1, nseg, 1, nseg - 1, 1, nseg - 1};
     }
     extern __shared__ __align__(16) float smem[];
@@ -196,9 +196,10 @@ cudaError_t launch_segment_scan(const float* s0, const float* m, float* sin, flo
 }
 
 cudaError_t launch_segment_scan_planned(const float* s0, const float* m, float* sin, float* hT,
-                                        int BH, const int* plan, cudaStream_t stream) {
+                                        int BH, int nseg_max, const int* plan,
+                                        cudaStream_t stream) {
     const ScanLayout L{1, 1, 1, 1, 1, 1};  // replaced from the plan in the kernel
-    return launch_scan(s0, m, sin, hT, BH, 1, L, stream, plan, true);
+    return launch_scan(s0, m, sin, hT, BH, nseg_max, L, stream, plan, true);
 }
 
 cudaError_t launch_slice_scan(const float* s0, const float* m, float* sin, float* hT, int BH,
