@@ -95,7 +95,7 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
     if ((long long)B * H >= (1LL << 31)) return (size_t)-1;
     // The tensor-core path balances sequences over the SMs through a state
     // handoff buffer; the fp32 path and empty problems need nothing.
-    if (io != KDA_BF16 || dk != 128 || T == 0 || (long long)B * H < 2) return 0;
+    if (io != KDA_BF16 || T == 0 || (long long)B * H < 2) return 0;
     return kda::balanced_workspace_bytes((long long)B * H);
 }
 
@@ -278,7 +278,7 @@ kda_status_t chunk_fwd_impl(const void* q, const void* k, const void* v, const f
     a.ckpt_every = ckpt ? ckpt_every : 0;
     // A prefill workspace of the queried size enables the balanced schedule;
     // without one (or a smaller one) every sequence gets its own CTA.
-    if (bal_ws && nseg_eff <= 1 && io == KDA_BF16 && dk == 128) {
+    if (bal_ws && nseg_eff <= 1 && io == KDA_BF16) {
         const size_t need = kda::balanced_workspace_bytes((long long)B * H);
         if (bal_bytes < need) {
             bal_ws = nullptr;

@@ -430,13 +430,20 @@ __device__ __forceinline__ void solve_level3(float* FA, const float* FT, int war
 
 // SEG: the kernel serves the segment and correction passes (runtime task
 // decode); the whole-sequence instantiation compiles without any of it.
-template <bool SEG>
+// DIO: channels of the caller's q, k, v, g, o, h0, hT and ckpt. 128, or 64
+// (whole sequences only), run as d = 128 with channels 64..127 zero: the
+// tensor maps fill them with zeros on load and clip them on store, and the
+// state's rows and columns past DIO stay exactly zero (k, v = 0 there and the
+// decay e^0 = 1 keeps a zero row or column zero), so only the caller's state
+// tensors need the stride DIO.
+template <bool SEG, int DIO>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
                         const __grid_constant__ CUtensorMap map_g,
                         const __grid_constant__ CUtensorMap map_o, const TcParams p) {
+    static_assert(DIO == kD || (DIO == 64 && !SEG), "d = 64 runs whole sequences only");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // Align to 1024 bytes (the 128-byte swizzle atom) by offsetting the
     // __shared__ array itself, so every access below stays an LDS/STS: an
@@ -501,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // segments), the identity (transition runs) or the incoming state.
     const float* h0p = (kind == 2 && whole) ? p.ws_sin + (size_t)bh * kD * kD
                        : kind == 2 ? p.ws_sin + ((size_t)bh * (nseg - 1) + seg - 1) * kD * kD
-                       : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * kD * kD
+                       : (kind == 0 && seg == 0 && p.h0) ? p.h0 + (size_t)bh * DIO * DIO
                                                          : nullptr;
     int nchunks = whole
                       ? (T + kC - 1) / kC
@@ -551,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         t_begin = c0 * kC;
         nchunks = c1 - c0;
         h0p = from_slot ? p.bal_states + (size_t)bh * kD * kD
-              : p.h0    ? p.h0 + (size_t)bh * kD * kD
+              : p.h0    ? p.h0 + (size_t)bh * DIO * DIO
                         : nullptr;
     };
     if (bal && ntask > 0) set_task(0);
@@ -719,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = 32 * u + e;
             x[e] = kind == 1 ? (lane == i ? 1.f : 0.f)
                    : from_slot ? __ldcg(h0p + (size_t)i * kD + lane)
-                   : (h0p ? h0p[(size_t)i * kD + lane] : 0.f);
+                   : (h0p && (DIO == kD || (i < DIO && lane < DIO)) ? h0p[(size_t)i * DIO + lane] : 0.f);
         }
         tmem_st16(tq + TM_S + 32 * u, x);
         tmem_st16(tq + TM_S + 32 * u + 16, x + 16);
@@ -1209,13 +1216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.ckpt && (c + 1) % p.ck_chunks == 0 && (c + 1) / p.ck_chunks <= p.n_ckpt) {
             if (__syncthreads_or(!r4_wait())) { failed = true; break; }
             const int jc = (c + 1) / p.ck_chunks - 1;
-            float* dst = p.ckpt + ((size_t)blockIdx.x * p.n_ckpt + jc) * kD * kD + lane;
+            float* dst = p.ckpt + ((size_t)blockIdx.x * p.n_ckpt + jc) * DIO * DIO + lane;
 #pragma unroll
             for (int cc = 0; cc < 32; cc += 16) {
                 float x[16];
-                tmem_ld16(tq + TM_S + 32 * u + cc, x);
+                tmem_ld16(tq + TM_S + 32 * u + cc, x);  // warp-collective: every warp loads
 #pragma unroll
-                for (int jj = 0; jj < 16; jj++) dst[(size_t)(32 * u + cc + jj) * kD] = x[jj];
+                for (int jj = 0; jj < 16; jj++)
+                    if (DIO == kD || (lane < DIO && 32 * u + cc + jj < DIO))
+                        dst[(size_t)(32 * u + cc + jj) * DIO] = x[jj];
             }
             tc_fence_before();
         }
@@ -1243,22 +1252,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bh2, seg2;
         task_seq(&bh2, &seg2);
         if (bal) hTp = to_slot ? p.bal_states + (size_t)bh * kD * kD
-                       : p.hT  ? p.hT + (size_t)bh * kD * kD
+                       : p.hT  ? p.hT + (size_t)bh * DIO * DIO
                                : nullptr;
-        else if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * kD * kD : nullptr;
+        else if (!SEG || p.pass == 0) hTp = p.hT ? p.hT + (size_t)bh2 * DIO * DIO : nullptr;
         else if (p.pass == 3) hTp = p.ws_m + (size_t)bh2 * kD * kD;
         else if (p.pass == 4) hTp = nullptr;
         else if (kind == 0) hTp = p.ws_s0 + ((size_t)bh2 * nseg + seg2) * kD * kD;
         else if (kind == 1) hTp = p.ws_m + ((size_t)bh2 * (nseg - 1) + seg2 - 1) * kD * kD;
     }
     if (hTp && !failed) {
+        // the caller's hT at stride DIO; the handoff slots and the segment
+        // workspace at kD (the segmented passes run only at DIO = kD)
+        const int ld = to_slot ? kD : DIO;
         float* dst = hTp + lane;
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 16) {
             float x[16];
-            tmem_ld16(tq + TM_S + 32 * u + cc, x);
+            tmem_ld16(tq + TM_S + 32 * u + cc, x);  // warp-collective: every warp loads
 #pragma unroll
-            for (int jj = 0; jj < 16; jj++) dst[(size_t)(32 * u + cc + jj) * kD] = x[jj];
+            for (int jj = 0; jj < 16; jj++)
+                if (DIO == kD || (lane < ld && 32 * u + cc + jj < ld))
+                    dst[(size_t)(32 * u + cc + jj) * ld] = x[jj];
         }
     }
     gc += nchunks;
@@ -1319,11 +1333,14 @@ struct TcMaps {
 
 bool make_maps(TcMaps* m, const ChunkFwdArgs& a) {
     if (a.T == 0) return true;
-    return make_map(&m->q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
-           make_map(&m->k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
-           make_map(&m->v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, 64) &&
-           make_map(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.H, kD, 32) &&
-           (!a.o || make_map(&m->o, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, kD, kD,
+    // The caller's channel count (128, or 64 with the boxes still covering
+    // 128 channels: zero-filled past the tensor on load, clipped on store).
+    const int d = a.dk;
+    return make_map(&m->q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, d, 64) &&
+           make_map(&m->k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, d, 64) &&
+           make_map(&m->v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, d, 64) &&
+           make_map(&m->g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.H, d, 32) &&
+           (!a.o || make_map(&m->o, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B, a.T, a.H, d, kD,
                              CU_TENSOR_MAP_SWIZZLE_NONE));
 }
 
@@ -1346,14 +1363,14 @@ TcParams base_params(const ChunkFwdArgs& a) {
 
 // dependent: launch as a programmatic dependent of the stream's previous
 // kernel (its launch overlaps that kernel's end; the kernel waits for it).
-template <bool SEG>
+template <bool SEG, int DIO = kD>
 cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaStream_t stream,
                       bool dependent = false) {
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel<SEG>,
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel<SEG, DIO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (!dependent) {
-        kda_chunk_tc_kernel<SEG><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(
+        kda_chunk_tc_kernel<SEG, DIO><<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(
             m.q, m.k, m.v, m.g, m.o, p);
         return cudaGetLastError();
     }
@@ -1367,23 +1384,22 @@ cudaError_t launch_tc(const TcMaps& m, const TcParams& p, long long grid, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kda_chunk_tc_kernel<SEG>, m.q, m.k, m.v, m.g, m.o, p);
+    return cudaLaunchKernelEx(&cfg, kda_chunk_tc_kernel<SEG, DIO>, m.q, m.k, m.v, m.g, m.o, p);
 }
-
-}  // namespace
 
 // Balanced schedule (see TcParams::bal_W): when B * H sequences do not fill
 // whole waves of one CTA per SM, one cooperative launch of (at most) one CTA
 // per SM gives every CTA the same number of chunk steps. Returns
 // cudaErrorNotSupported when the plain schedule should run instead.
+template <int DIO>
 cudaError_t launch_balanced(const TcMaps& m, const ChunkFwdArgs& a) {
     if (!a.bal_ws || a.ckpt || a.T <= 0) return cudaErrorNotSupported;
     int dev = 0, nsm = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(kda_chunk_tc_kernel<false>,
+        cudaFuncSetAttribute(kda_chunk_tc_kernel<false, DIO>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_chunk_tc_kernel<false>, kThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_chunk_tc_kernel<false, DIO>, kThreads,
                                                       SMEM_BYTES) != cudaSuccess ||
         nsm <= 0 || per_sm <= 0) {
         cudaGetLastError();
@@ -1414,7 +1430,7 @@ cudaError_t launch_balanced(const TcMaps& m, const ChunkFwdArgs& a) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kda_chunk_tc_kernel<false>, m.q, m.k, m.v, m.g, m.o, p);
+    e = cudaLaunchKernelEx(&cfg, kda_chunk_tc_kernel<false, DIO>, m.q, m.k, m.v, m.g, m.o, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cudaErrorNotSupported;
@@ -1422,13 +1438,22 @@ cudaError_t launch_balanced(const TcMaps& m, const ChunkFwdArgs& a) {
     return cudaSuccess;
 }
 
-cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
-    if (a.dk != kD || a.dv != kD) return launch_chunk_fwd_simt(a, KDA_BF16);
+template <int DIO>
+cudaError_t launch_whole(const ChunkFwdArgs& a) {
     TcMaps m;
     if (!make_maps(&m, a)) return cudaErrorInvalidValue;
-    const cudaError_t e = launch_balanced(m, a);
+    const cudaError_t e = launch_balanced<DIO>(m, a);
     if (e != cudaErrorNotSupported) return e;
-    return launch_tc<false>(m, base_params(a), (long long)a.B * a.H, a.stream);
+    return launch_tc<false, DIO>(m, base_params(a), (long long)a.B * a.H, a.stream);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fwd_tc(const ChunkFwdArgs& a) {
+    if (a.dv != a.dk) return launch_chunk_fwd_simt(a, KDA_BF16);
+    if (a.dk == kD) return launch_whole<kD>(a);
+    if (a.dk == 64) return launch_whole<64>(a);
+    return launch_chunk_fwd_simt(a, KDA_BF16);
 }
 
 cudaError_t launch_chunk_fwd_tc_slice(const ChunkFwdArgs& a, int which, float* state) {

@@ -90,8 +90,8 @@ const char* kda_last_error_string(void);
 
 /*
  * Bytes of device workspace that let kda_chunk_fwd balance the work over the
- * SMs: B*H*dk*dv*4 bytes of states plus B*H ints (rounded up to 256 bytes) for
- * io = KDA_BF16 with dk = dv = 128, T > 0 and B*H >= 2; 0 otherwise (the fp32
+ * SMs: B*H*128*128*4 bytes of states plus B*H ints (rounded up to 256 bytes)
+ * for io = KDA_BF16 (dk = dv = 64 or 128), T > 0 and B*H >= 2; 0 otherwise (the fp32
  * path keeps nothing off chip). With a buffer of at least this size the
  * tensor-core path may run one CTA per SM over the sequences laid end to end,
  * a sequence split between two CTAs handing its state over through the
@@ -126,9 +126,11 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
  *   d_status : device int or NULL              (in/out, OR-ed KDA_DEV_* bits)
  *   stream : cudaStream_t
  *
- * io = KDA_BF16 with dk = dv = 128 runs the tensor-core (tcgen05/TMEM) path
- * with fp32 state; io = KDA_F32 (and bf16 with dk = dv = 64, whose tiles the
- * tensor-core kernel does not implement) runs an fp32 CUDA-core path, untuned,
+ * io = KDA_BF16 runs the tensor-core (tcgen05/TMEM) path with fp32 state; at
+ * dk = dv = 64 it runs as dk = dv = 128 with channels 64..127 zero (the tensor
+ * maps fill them with zeros on load and clip them on store, so the bytes moved
+ * are those of d = 64 and the results exactly those of d = 64; the arithmetic
+ * is that of d = 128). io = KDA_F32 runs an fp32 CUDA-core path, untuned,
  * meant for accuracy rather than speed. With a
  * full-size workspace the tensor-core path enqueues a memset of the handoff
  * flags before its (cooperative) launch.

@@ -50,6 +50,8 @@ def test_workspace_size(L):
     assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 128, 128, kda.KDA_BF16) == 256 * 65536 + 1024
     assert L.kda_chunk_fwd_workspace_size(3, 64, 100, 128, 128, kda.KDA_BF16) == 300 * 65536 + 1280
     assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 128, 128, kda.KDA_F32) == 0
+    # bf16 d = 64 runs the same kernel at d = 128: the same handoff buffer
+    assert L.kda_chunk_fwd_workspace_size(8, 8192, 32, 64, 64, kda.KDA_BF16) == 256 * 65536 + 1024
     assert L.kda_chunk_fwd_workspace_size(8, 0, 32, 128, 128, kda.KDA_BF16) == 0
     assert L.kda_chunk_fwd_workspace_size(1, 64, 1, 128, 128, kda.KDA_BF16) == 0
     bad = ctypes.c_size_t(-1).value

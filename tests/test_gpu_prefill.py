@@ -177,8 +177,8 @@ def test_status_flags(io, bad, flag):
 @pytest.mark.parametrize("bad", [float("nan"), float("inf")])
 def test_nonfinite_qkv_is_flagged(io, d, name, bad):
     """A NaN or Inf in q, k or v (here in the second chunk of one head, on the
-    tensor-core path for bf16 d=128 and the CUDA-core path otherwise) sets
-    KDA_DEV_NONFINITE."""
+    tensor-core path for bf16, d = 64 or 128, and the CUDA-core path for fp32)
+    sets KDA_DEV_NONFINITE."""
     w = small(io, d, True)
     x = inputs.prefill_inputs(w, DEV, B=2, T=150, H=2, seed=19)
     x[name][1, 97, 0, 11] = bad
@@ -305,3 +305,45 @@ def test_chunk_size_invariance():
     o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
     assert_o(o32, o_ref, torch.float32, "C=32 o")
     assert_s(h32, h_ref, torch.float32, "C=32 hT")
+
+
+@pytest.mark.parametrize("B,T,H,h0", [(1, 1, 2, True), (2, 129, 3, False), (1, 1000, 4, True),
+                                      (3, 333, 2, True)])
+def test_bf16_d64_on_tensor_cores(B, T, H, h0):
+    """bf16 with d = 64 runs the tensor-core kernel at d = 128, channels 64..127
+    read as zeros and clipped on store: outputs and final state against the
+    oracle, ragged lengths, with and without h0."""
+    w = inputs.PrefillWorkload("d64", B, T, H, 64, 64, "bf16", 80 + T, h0_std=0.02 if h0 else None)
+    x = inputs.prefill_inputs(w, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, hT = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    xc = {n: (t.cpu() if t is not None else None) for n, t in x.items()}
+    o_ref, h_ref = oracle.prefill(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["h0"])
+    assert_o(o, o_ref, torch.bfloat16)
+    assert_s(hT, h_ref, torch.bfloat16)
+
+
+def test_bf16_d64_balanced_and_aliased():
+    """d = 64 with more sequences than SMs: the balanced schedule (handoffs in
+    the 128 x 128 internal layout) gives the bits of one CTA per sequence, hT
+    may alias h0, and a batch row matches the oracle."""
+    B, T, H = 2, 1280, 80  # 160 sequences of 20 chunks
+    w = inputs.PrefillWorkload("d64b", B, T, H, 64, 64, "bf16", 90, h0_std=0.02)
+    x = inputs.prefill_inputs(w, DEV)
+    ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(B, T, H, 64, 64, torch.bfloat16),
+                     dtype=torch.uint8, device=DEV)
+    assert ws.numel() > 0
+    o_b, h_b = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], workspace=ws)
+    o_p, h_p = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    h = x["h0"].clone()
+    o_a, h_a = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h, hT=h)
+    torch.cuda.synchronize()
+    assert torch.equal(o_b, o_p) and torch.equal(h_b, h_p)
+    assert torch.equal(o_a, o_p) and torch.equal(h_a, h_p) and h_a.data_ptr() == h.data_ptr()
+    sub = {n: t[0:1, :, 0:4].contiguous().cpu() for n, t in x.items() if n != "h0"}
+    o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                                  x["h0"][0:1, 0:4].contiguous().cpu())
+    assert_o(o_b[0:1, :, 0:4], o_ref, torch.bfloat16)
+    assert_s(h_b[0:1, 0:4], h_ref, torch.bfloat16)
