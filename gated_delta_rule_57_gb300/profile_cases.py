@@ -4,6 +4,7 @@
     python -m gated_delta_rule_57_gb300.profile_cases decode  [--calls 4]
     python -m gated_delta_rule_57_gb300.profile_cases spec    [--calls 4]
     python -m gated_delta_rule_57_gb300.profile_cases long    [--T 65536] [--nseg 5|decay] [--calls 4]
+    python -m gated_delta_rule_57_gb300.profile_cases t4k     [--nseg 4|decay|1] [--calls 4]
 
 Draws the seeded synthetic inputs on the GPU, then makes `calls` back-to-back
 calls of kda_chunk_fwd (prefill: B x 8192 tokens x 32 heads, d = 128, bf16)
@@ -11,7 +12,8 @@ or kda_decode_step (256 sequences x 32 heads, d = 128), or rounds of
 kda_decode_multi (the same 256 x 32 states, 4 draft tokens: verify then
 commit), or kda_chunk_fwd_segmented (long: one sequence of T tokens x 32 heads
 split into nseg segments; three launches per call; --nseg decay plans the
-split on the device from the decay probe: five launches). Under a profiler,
+split on the device from the decay probe: five launches; t4k: the same on
+one sequence of 4096 tokens x 32 heads, half of them with g = -4.99). Under a profiler,
 skip the first calls as warm-up (e.g. ncu -s 2 -c 1 -k regex:kda_).
 """
 import argparse
@@ -23,7 +25,7 @@ from . import inputs, kda
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("which", choices=["prefill", "decode", "spec", "long"])
+    ap.add_argument("which", choices=["prefill", "decode", "spec", "long", "t4k"])
     ap.add_argument("--B", type=int, default=8)
     ap.add_argument("--T", type=int, default=65536)
     ap.add_argument("--nseg", default="5", help="segment count, or 'decay'")
@@ -42,8 +44,11 @@ def main():
         x = inputs.decode_inputs(w, dev, steps=args.calls)
         for s in range(args.calls):
             kda.kda_decode_step(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], x["S"])
-    elif args.which == "long":
-        w = inputs.PREFILL_T1M
+    elif args.which in ("long", "t4k"):
+        # t4k: B=1, T=4096, H=32 with the stress heads (g = -4.99); --T is ignored
+        w = inputs.PREFILL_T1M if args.which == "long" else inputs.PREFILL_T4K
+        if args.which == "t4k":
+            args.T = w.T
         x = inputs.prefill_inputs(w, dev, T=args.T)
         o = torch.empty_like(x["v"])
         hT = torch.empty(w.B, w.H, w.dk, w.dv, device=dev)
