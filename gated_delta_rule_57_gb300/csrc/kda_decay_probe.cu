@@ -15,27 +15,28 @@
 // only). The planner takes the largest entry as the decay per chunk that the
 // sequences can be counted on; it is an estimate from a sample, so it guides
 // the plan only: results never depend on it. A CTA takes one sample of one
-// batch row for eight heads; four warps per head read 16 of the chunk's rows
-// each (dk contiguous floats per row), all loads in flight before any is used,
-// and the four partial sums are added in token order.
+// batch row for hpc heads (2, so that a few heads still spread over the SMs;
+// 8 when H needs it to fit the grid); four warps per head read 16 of the
+// chunk's rows each (dk contiguous floats per row), all loads in flight before
+// any is used, and the four partial sums are added in token order.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kProbeHeads = 8;   // heads per CTA
+constexpr int kProbeHeads = 8;   // most heads per CTA
 constexpr int kProbeParts = 4;   // warps per head, 16 tokens each
 constexpr int kProbeRows = 16;   // rows of g in flight per warp
 
 template <int DK>
 __global__ void __launch_bounds__(32 * kProbeHeads * kProbeParts)
-    kda_decay_probe_kernel(const float* __restrict__ g, int T, int H, int nsample,
+    kda_decay_probe_kernel(const float* __restrict__ g, int T, int H, int nsample, int hpc,
                            float* __restrict__ out) {
     constexpr int PER = DK / 32;  // floats per lane of a row: 4 or 2
     __shared__ float s_part[kProbeHeads][kProbeParts];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hl = warp / kProbeParts, part = warp % kProbeParts;
-    const int s = blockIdx.x, b = blockIdx.y, h = blockIdx.z * kProbeHeads + hl;
+    const int s = blockIdx.x, b = blockIdx.y, h = blockIdx.z * hpc + hl;
     const int nch = (T + 63) / 64;
     const int c = (int)(((long long)s * nch) / nsample);
     const int t0 = c * 64 + part * kProbeRows, t1 = min(T, c * 64 + 64);
@@ -85,8 +86,8 @@ __global__ void __launch_bounds__(32 * kProbeHeads * kProbeParts)
     }
     if (lane == 0) s_part[hl][part] = sum;
     __syncthreads();
-    if (threadIdx.x < kProbeHeads) {
-        const int hh = blockIdx.z * kProbeHeads + threadIdx.x;
+    if ((int)threadIdx.x < hpc) {
+        const int hh = blockIdx.z * hpc + threadIdx.x;
         if (hh < H) {
             float tot = 0.f;
 #pragma unroll
@@ -181,12 +182,13 @@ __global__ void __launch_bounds__(kPlanThreads)
 
 cudaError_t launch_decay_probe(const float* g, int B, int T, int H, int dk, int nsample,
                                float* out, cudaStream_t stream) {
-    const dim3 grid((unsigned)nsample, (unsigned)B, (unsigned)((H + kProbeHeads - 1) / kProbeHeads));
-    constexpr int threads = 32 * kProbeHeads * kProbeParts;
+    const int hpc = (H + 1) / 2 <= 65535 ? 2 : kProbeHeads;
+    const dim3 grid((unsigned)nsample, (unsigned)B, (unsigned)((H + hpc - 1) / hpc));
+    const int threads = 32 * hpc * kProbeParts;
     if (dk == 128)
-        kda_decay_probe_kernel<128><<<grid, threads, 0, stream>>>(g, T, H, nsample, out);
+        kda_decay_probe_kernel<128><<<grid, threads, 0, stream>>>(g, T, H, nsample, hpc, out);
     else
-        kda_decay_probe_kernel<64><<<grid, threads, 0, stream>>>(g, T, H, nsample, out);
+        kda_decay_probe_kernel<64><<<grid, threads, 0, stream>>>(g, T, H, nsample, hpc, out);
     return cudaGetLastError();
 }
 

@@ -17,7 +17,12 @@
 // exchange between them; a CTA prefetches the next segment's M and its block
 // of S0 (cp.async, two buffers) while it multiplies the current ones. fp32
 // throughout; every output element starts from S0 and adds M[i][kk] X[kk][j]
-// for kk = 0, 1, .., dk - 1 in that order, whatever the blocking.
+// for kk = 0, 1, .., dk - 1 in that order, whatever the blocking. A transition
+// that is exactly zero (a segment whose decay empties any state: its run
+// stopped at a zero state) with a finite X adds only zeros, so that step
+// keeps X_{s+1} = S0_s without the product (equal values; only the sign of a
+// zero entry may differ from adding the zero products); a NaN or Inf in M or
+// X takes the product, so it propagates as before.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -121,30 +126,42 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         __syncthreads();  // M_s, S0_s and X visible to every thread
         const float* Ms = Mb + b * kMFloats;
         const float* Ss = Sb + b * kBFloats;
+        bool need = false;  // a nonzero (or NaN) entry of M_s, or a non-finite one of X
+        for (int e = tid; e < kDs * kDs / 4; e += kScanThreads) {
+            const float4 f = *reinterpret_cast<const float4*>(Ms + (e >> 5) * kLdm + 4 * (e & 31));
+            need = need || f.x != 0.f || f.y != 0.f || f.z != 0.f || f.w != 0.f;
+        }
+        for (int e = tid; e < kBFloats / 4; e += kScanThreads) {
+            const float4 f = *reinterpret_cast<const float4*>(X + 4 * e);
+            need = need || !isfinite(f.x) || !isfinite(f.y) || !isfinite(f.z) || !isfinite(f.w);
+        }
+        need = __syncthreads_or(need);
         float acc[8][4];
 #pragma unroll
         for (int a = 0; a < 8; a++) {
             const float4 f = *reinterpret_cast<const float4*>(Ss + (i0 + 16 * a) * kCols + j0);
             acc[a][0] = f.x; acc[a][1] = f.y; acc[a][2] = f.z; acc[a][3] = f.w;
         }
+        if (need) {
 #pragma unroll 2
-        for (int kk = 0; kk < kDs; kk += 4) {
-            float4 mv[8], xv[4];
+            for (int kk = 0; kk < kDs; kk += 4) {
+                float4 mv[8], xv[4];
 #pragma unroll
-            for (int a = 0; a < 8; a++)
-                mv[a] = *reinterpret_cast<const float4*>(Ms + (i0 + 16 * a) * kLdm + kk);
+                for (int a = 0; a < 8; a++)
+                    mv[a] = *reinterpret_cast<const float4*>(Ms + (i0 + 16 * a) * kLdm + kk);
 #pragma unroll
-            for (int q = 0; q < 4; q++)
-                xv[q] = *reinterpret_cast<const float4*>(X + (kk + q) * kCols + j0);
+                for (int q = 0; q < 4; q++)
+                    xv[q] = *reinterpret_cast<const float4*>(X + (kk + q) * kCols + j0);
 #pragma unroll
-            for (int a = 0; a < 8; a++) {
-                const float mm[4] = {mv[a].x, mv[a].y, mv[a].z, mv[a].w};
+                for (int a = 0; a < 8; a++) {
+                    const float mm[4] = {mv[a].x, mv[a].y, mv[a].z, mv[a].w};
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    acc[a][0] = fmaf(mm[q], xv[q].x, acc[a][0]);
-                    acc[a][1] = fmaf(mm[q], xv[q].y, acc[a][1]);
-                    acc[a][2] = fmaf(mm[q], xv[q].z, acc[a][2]);
-                    acc[a][3] = fmaf(mm[q], xv[q].w, acc[a][3]);
+                    for (int q = 0; q < 4; q++) {
+                        acc[a][0] = fmaf(mm[q], xv[q].x, acc[a][0]);
+                        acc[a][1] = fmaf(mm[q], xv[q].y, acc[a][1]);
+                        acc[a][2] = fmaf(mm[q], xv[q].z, acc[a][2]);
+                        acc[a][3] = fmaf(mm[q], xv[q].w, acc[a][3]);
+                    }
                 }
             }
         }

@@ -105,6 +105,27 @@ def test_segmented_nonfinite_qkv_is_flagged(name):
     assert st & kda.KDA_DEV_NONFINITE
 
 
+def test_nan_crosses_zero_transitions():
+    """g = -4.99 everywhere: every transition is exactly zero, so the scan
+    takes X_{s+1} = S0_s without the product. A NaN in v in the first segment
+    must still reach every later segment, as in the single pass (a zero
+    transition times a NaN state is NaN): the same NaN entries in o and hT,
+    the flag set, and the clean head against the oracle."""
+    x = inputs.prefill_inputs(workload(False), DEV, B=1, T=1024, H=2, seed=17)
+    x["g"].fill_(-4.99)
+    x["v"][0, 5, 1, 40] = float("nan")
+    o1, h1 = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    o, hT, st = run_seg(x, 4)
+    assert st & kda.KDA_DEV_NONFINITE
+    assert torch.equal(torch.isnan(o), torch.isnan(o1))
+    assert torch.equal(torch.isnan(hT), torch.isnan(h1))
+    assert torch.isnan(o[0, -1, 1, 40]) and torch.isnan(hT[0, 1, :, 40]).all()
+    sub = {n: x[n][:, :, :1].contiguous().cpu() for n in ("q", "k", "v", "g", "beta")}
+    o_ref, h_ref = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None)
+    assert_o(o[:, :, :1], o_ref, BF16)
+    assert_s(hT[:, :1], h_ref, BF16)
+
+
 @pytest.mark.slow
 def test_t1m_benchmark_calls_against_oracle():
     """The long-context workload (B=1, T=2^20, H=32, the benchmark's seed)
