@@ -129,8 +129,8 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, kda_dty
  * io = KDA_BF16 runs the tensor-core (tcgen05/TMEM) path with fp32 state; at
  * dk = dv = 64 it runs as dk = dv = 128 with channels 64..127 zero (the tensor
  * maps fill them with zeros on load and clip them on store, so the bytes moved
- * are those of d = 64 and the results exactly those of d = 64; the arithmetic
- * is that of d = 128). io = KDA_F32 runs an fp32 CUDA-core path, untuned,
+ * are those of d = 64 and the zero channels add only exact zeros to every sum;
+ * the arithmetic is that of d = 128). io = KDA_F32 runs an fp32 CUDA-core path, untuned,
  * meant for accuracy rather than speed. With a
  * full-size workspace the tensor-core path enqueues a memset of the handoff
  * flags before its (cooperative) launch.
