@@ -80,9 +80,9 @@ def test_workload_b8_t8192():
     check_against_oracle(x, o, hT, torch.bfloat16)
 
 
-@pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_empty_sequence_returns_h0(io):
-    w = small(io, 128, True)
+@pytest.mark.parametrize("io,d", [("bf16", 128), ("bf16", 64), ("f32", 128)])
+def test_empty_sequence_returns_h0(io, d):
+    w = small(io, d, True)
     x = inputs.prefill_inputs(w, DEV, B=2, T=0, H=3)
     o, hT = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
     torch.cuda.synchronize()
