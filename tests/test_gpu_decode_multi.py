@@ -94,6 +94,36 @@ def test_decay_at_its_bound_over_long_drafts():
     assert_s(S, h_ref, torch.float32)
 
 
+@pytest.mark.parametrize("io,K", [("bf16", 4), ("f32", 6)])
+def test_commit_many_heads_mixed_lengths(io, K):
+    """2400 heads (several waves of CTAs) with accepted lengths 0..K mixed,
+    a run of sequences with none: those keep their state bit for bit, and
+    sampled sequences match the oracle."""
+    N, H, d = 600, 4, 128
+    x = draft(N, K, H, d, io, 26 + K)
+    gen = torch.Generator().manual_seed(27 + K)
+    m_all = torch.randint(0, K + 1, (N,), generator=gen, dtype=torch.int32)
+    m_all[:40] = 0  # a run of sequences with nothing to apply
+    ntok = m_all.to(DEV)
+    S = x["h0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], S, ntok=ntok, commit=True,
+                         want_o=False, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    zero = (m_all == 0).nonzero().flatten().tolist()
+    assert torch.equal(S[zero], x["h0"][zero])
+    xc = {n: t.cpu() for n, t in x.items()}
+    for n in [40, 41, 151, 152, 303, 455, 598, 599]:
+        m = int(m_all[n])
+        if m == 0:
+            continue
+        sl = slice(n, n + 1)
+        _, h_ref = oracle.prefill(xc["q"][sl, :m], xc["k"][sl, :m], xc["v"][sl, :m],
+                                  xc["g"][sl, :m], xc["beta"][sl, :m], xc["h0"][sl])
+        assert_s(S[sl], h_ref, inputs.io_dtype(io), f"sequence {n}, {m} accepted tokens")
+
+
 def test_commit_all_equals_single_steps():
     N, K, H, d = 4, 4, 3, 128
     x = draft(N, K, H, d, "bf16", 23)
