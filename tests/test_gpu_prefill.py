@@ -347,3 +347,42 @@ def test_bf16_d64_balanced_and_aliased():
                                   x["h0"][0:1, 0:4].contiguous().cpu())
     assert_o(o_b[0:1, :, 0:4], o_ref, torch.bfloat16)
     assert_s(h_b[0:1, 0:4], h_ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,T,H,bal", [(2, 333, 3, False), (2, 1280, 80, True)])
+def test_bf16_d64_equals_zero_padded_d128(B, T, H, bal):
+    """bf16 d = 64 runs the d = 128 arithmetic on channels that the tensor maps
+    fill with zeros, so it gives exactly the bits of the d = 128 kernel on the
+    same inputs padded with zeros to 128 channels (g = 0 there), o and hT cut
+    back to 64: one CTA per sequence and the balanced schedule."""
+    w = inputs.PrefillWorkload("d64p", B, T, H, 64, 64, "bf16", 95 + T, h0_std=0.02)
+    x = inputs.prefill_inputs(w, DEV)
+
+    def pad(t, dims):
+        out = torch.zeros(*t.shape[:-dims], *([128] * dims), dtype=t.dtype, device=DEV)
+        out[(...,) + (slice(0, 64),) * dims] = t
+        return out
+
+    xp = {n: pad(x[n], 1) for n in ("q", "k", "v", "g")}
+    h0p = pad(x["h0"], 2)
+
+    def ws(d):
+        if not bal:
+            return None
+        return torch.zeros(kda.kda_chunk_fwd_workspace_size(B, T, H, d, d, torch.bfloat16),
+                           dtype=torch.uint8, device=DEV)
+
+    def call(q, k, v, g, h0, d):
+        o = torch.empty(B, T, H, d, dtype=torch.bfloat16, device=DEV)
+        hT = torch.empty(B, H, d, d, dtype=torch.float32, device=DEV)
+        w_ = ws(d)
+        if w_ is None:  # one CTA per sequence: a workspace too small for the balanced schedule
+            w_ = torch.empty(16, dtype=torch.uint8, device=DEV)
+        return kda.kda_chunk_fwd(q, k, v, g, x["beta"], h0, o=o, hT=hT, workspace=w_)
+
+    o64, h64 = call(x["q"], x["k"], x["v"], x["g"], x["h0"], 64)
+    o128, h128 = call(xp["q"], xp["k"], xp["v"], xp["g"], h0p, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(o64, o128[..., :64])
+    assert torch.equal(h64, h128[..., :64, :64])
+    assert torch.count_nonzero(o128[..., 64:]) == 0 and torch.count_nonzero(h128[..., 64:, :]) == 0
