@@ -19,7 +19,8 @@ C-ABI call from pinned host buffers, every input uploaded and o, hT read back
 inside the timed region, pipelined by batch row over copy and compute streams;
 its "host_link" object times the step's input bytes going up as one copy and
 its output bytes coming down as another, at the same time, nothing else: the
-least time any step that moves them can take.
+least time any step that moves them can take. The e2e figure is the median
+over the timed steps of the pipeline's step period; every run is listed too.
 
 The cpu_baseline sample doubles as a parity check ("parity"): the kernel runs
 on every batch row the oracle timed and the errors against it are reported.
@@ -320,23 +321,31 @@ def time_prefill_e2e(xh, steps, warmup, device):
 
     link()
     # Nine timed runs of `steps` pipelined steps, each right after one timing
-    # of the link alone. The median run is the number; every run and its link
-    # time are reported, and the link fraction is the median of the per-run
-    # ratios. (On a shared machine the host link itself slows down in bursts
-    # of some hundred milliseconds after heavy GPU work: a run in a burst is
-    # slow, and so is the link timed beside it.)
-    runs, links = [], []
+    # of the link alone. Inside a run every step is timed too: an event on the
+    # upload stream before each step's first copy, so the interval between two
+    # marks is the pipeline's period (uploads of one step, overlapped with the
+    # compute and downloads of the step before). The median step is the
+    # number; every run, its link time and the step spread are reported. (On a
+    # shared machine the host link itself slows down for ~180 ms in every
+    # ~480 ms or so: a run of ten steps overlaps such a window more often than
+    # not, a single step much less often, so the median step resolves the
+    # undisturbed rate that the median run only hits by chance.)
+    runs, links, step_ms = [], [], []
     for _ in range(9):
         links.append(link())
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         start.record(s_in)
-        for _ in range(steps):
+        for i in range(steps):
+            marks[i].record(s_in)
             step()
+        marks[steps].record(s_in)
         end.record(s_out)
         torch.cuda.synchronize()
         runs.append(start.elapsed_time(end) / steps)
-    e2e_ms = statistics.median(runs)
+        step_ms += [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
+    e2e_ms = statistics.median(step_ms)
     del hb_in, db_in, hb_out, db_out
-    return e2e_ms, links, h2d, d2h, o_h, hT_h, runs
+    return e2e_ms, links, h2d, d2h, o_h, hT_h, runs, step_ms
 
 
 def time_decode(device, seed, warmup=10):
@@ -548,10 +557,10 @@ def run_ours(args):
 
     # end to end through the same call, pinned host buffers, copies timed
     xh = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "h0")}
-    e2e_ms, e2e_links, h2d, d2h, o_host, hT_host, e2e_runs = time_prefill_e2e(
+    e2e_ms, e2e_links, h2d, d2h, o_host, hT_host, e2e_runs, e2e_steps = time_prefill_e2e(
         xh, max(3, min(args.steps, 10)), 2, device)
     link_ms = statistics.median(e2e_links)
-    link_frac = statistics.median(l / r for l, r in zip(e2e_links, e2e_runs))
+    link_frac = link_ms / e2e_ms
     # the pipelined host round trip must reproduce the device-resident result exactly
     e2e_exact = bool(torch.equal(o_host, o_dev.cpu()) and torch.equal(hT_host, hT_dev.cpu()))
     link_ms = max_over_ranks(link_ms, world, device)
@@ -624,6 +633,13 @@ def run_ours(args):
             "e2e": {"value": job_value(tokens_per_rank, e2e_ms, world), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "pipelined_by_batch_row": True,
+                    "what": "median over the timed steps of the step period (an event on the "
+                            "upload stream before each step); runs_ms_per_step: each run of "
+                            "consecutive steps, start of its first upload to end of its last "
+                            "download, per step",
+                    "steps_timed": len(e2e_steps),
+                    "steps_slower_than_median_by_10pct": sum(t > 1.1 * e2e_ms for t in e2e_steps),
+                    "median_run_ms_per_step": statistics.median(e2e_runs),
                     "runs_ms_per_step": e2e_runs,
                     "best_run_ms_per_step": min(e2e_runs),
                     "runs_slower_than_best_by_10pct": sum(r > 1.1 * min(e2e_runs)
@@ -636,8 +652,8 @@ def run_ours(args):
                                   "what": "the step's input bytes up as one copy and its "
                                           "output bytes down as another, concurrently, nothing "
                                           "else: the floor of any step that moves them, timed "
-                                          "before each e2e run; frac = median over the runs of "
-                                          "that time / the run's step time"}},
+                                          "before each e2e run; frac = its median / the median "
+                                          "step"}},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "decode": {"workload": DECODE.name, "value": dec_gbs, "unit": "GB/s",
